@@ -1,0 +1,306 @@
+"""Plain CPU oracle for fine-grained (block-scaled) FP8 quantization and GEMM.
+
+TEST INFRASTRUCTURE. Only the tests, ``__graft_entry__.smoke()`` and the CPU
+baseline / reference arm of ``bench.py`` may import this module. The product
+path (the CUDA library and its Python binding) never calls it, and this module
+imports nothing from the product package: the two share no code.
+
+It is written to be slow and obviously correct: vectorised numpy for the
+element-wise steps, a library matmul (fp64) as the only contraction, and no
+blocking, fusion or reordering beyond what the method itself states.
+
+Sources (five web pages on DeepSeek-V3's FP8 training recipe; cited by page
+title, or by host name for the two pages that print no title):
+
+[WHY-BE]  why-be.co.kr board post (as_center, wr_id 61844):
+          - paragraph "Delayed quantization ... 1x128 activation tile or
+            128x128 weight block": online max-abs per tile, E4M3 on all
+            tensors, FP8 activation caching, ~2% max relative error at K=4096;
+          - paragraph "these activations can be transformed from an 1x128
+            quantization tile to an 128x1 tile in the backward pass ...
+            scaling factors ... integral power of 2".
+[OMG]     "OMG! The most effective Deepseek Ever!" (thedaegu.com):
+          - paragraph on grouping (small groups share exponent bits) and on
+            scaling the max-abs of the input to the FP8 maximum;
+          - paragraph on limited-precision Tensor Core accumulation, promotion
+            of partial results to FP32 registers on CUDA cores at a fixed
+            interval, dequantization folded into that promotion, and
+            Figure 6 (Fprop, Dgrad and Wgrad all in FP8).
+[FOOLED]  "Don't Be Fooled By Deepseek Chatgpt": paragraph on promotion to
+          CUDA cores for higher precision, Figure 7 (b).
+[HEARAON] hearaon.co.kr board post (wr_id 810961): paragraph "Higher FP8 GEMM
+          Accumulation Precision in Tensor Cores" (Hopper keeps 14 bits of
+          each aligned mantissa product).
+
+Readings taken where the pages are silent (each one is listed, with its
+reason, in the design notes of the repository):
+  * E4M3 is the "fn" variant: bias 7, no infinities, 0x7F/0xFF are NaN,
+    largest finite value 448.
+  * Encoding rounds to nearest, ties to the even code, and saturates to +-448.
+  * The stored scale is the dequantization scale s = RN32(amax / 448),
+    floored at 2**-126; codes are enc(RN32(x / s)). With the power-of-two
+    option, s = 2**p with p the smallest integer such that amax <= 448 * 2**p
+    (p >= -126).
+  * Promotion interval along K is 128 elements.
+  * Re-tiling (1x128 -> 128x1) starts from the cached codes and their scales,
+    dequantized exactly as RN32(dec(q) * s).
+
+parity pins: every public function here is pinned by tests/test_oracle.py
+against brute force, closed forms or library routines; none is unpinned.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+E4M3_MAX = 448.0
+TILE = 128  # the 1x128 / 128x1 / 128x128 tile edge [WHY-BE]
+F32_MIN_NORMAL = np.float32(2.0 ** -126)
+
+
+# ---------------------------------------------------------------------------
+# E4M3 code <-> value
+# ---------------------------------------------------------------------------
+def e4m3_decode(codes) -> np.ndarray:
+    """Value of each E4M3 code, as float64.
+
+    E4M3 = 1 sign bit, 4 exponent bits (bias 7), 3 mantissa bits [WHY-BE,
+    paragraph on E4M3 for all tensors]. Exponent field 0 is subnormal:
+    m/8 * 2**-6. Codes 0x7F and 0xFF are NaN; there is no infinity.
+    """
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    e = (c >> 3) & 0xF
+    m = (c & 0x7).astype(np.float64)
+    mag = np.where(e == 0, m / 8.0 * 2.0 ** -6,
+                   (1.0 + m / 8.0) * np.exp2(e.astype(np.float64) - 7.0))
+    mag = np.where((c & 0x7F) == 0x7F, np.nan, mag)
+    return np.where((c & 0x80) != 0, -mag, mag)
+
+
+# The 127 non-negative finite E4M3 values in increasing order; index == code.
+_E4M3_NONNEG = e4m3_decode(np.arange(0, 127, dtype=np.uint8))
+
+
+def e4m3_encode(v) -> np.ndarray:
+    """Nearest E4M3 code of each float32 value: ties go to the even code,
+    magnitudes above 448 saturate to 448, the sign is kept (so -0 and negative
+    values that round to zero give 0x80).
+
+    Written as a table search: with lo/hi the two neighbouring representable
+    magnitudes, compare |v| with their midpoint (exact in float64: both
+    neighbours have 4 significant bits). Codes of non-negative values are
+    ordered like the values, so "even mantissa" is "even code".
+    """
+    v = np.asarray(v, dtype=np.float32)
+    if np.isnan(v).any():
+        raise ValueError("NaN input is outside the oracle's domain")
+    a = np.abs(v).astype(np.float64)
+    lo = np.searchsorted(_E4M3_NONNEG, a, side="right") - 1
+    lo = np.clip(lo, 0, 126)
+    hi = np.minimum(lo + 1, 126)
+    mid = (_E4M3_NONNEG[lo] + _E4M3_NONNEG[hi]) / 2.0
+    tie_even = np.where(lo % 2 == 0, lo, hi)
+    code = np.where(a < mid, lo, np.where(a > mid, hi, tie_even))
+    code = np.where(lo == hi, lo, code)  # at or above 448: saturate
+    return (code | np.where(np.signbit(v), 0x80, 0)).astype(np.uint8)
+
+
+# ---------------------------------------------------------------------------
+# Scale of a tile from its max-abs
+# ---------------------------------------------------------------------------
+def tile_scale(amax, pow2: bool) -> np.ndarray:
+    """Dequantization scale of a tile from its online max-abs.
+
+    The max-abs of the tile is mapped onto the largest FP8 value [OMG,
+    paragraph on aligning the input's max-abs with the FP8 maximum;
+    WHY-BE, paragraph "we calculate the maximum absolute value online for
+    each 1x128 activation tile or 128x128 weight block ... derive the scaling
+    factor"].
+
+    default: s = RN32(amax / 448), floored at 2**-126 so that an all-zero
+             tile still has a finite, positive scale.
+    pow2:    s = 2**p, p the smallest integer with amax <= 448 * 2**p, floored
+             at -126 [WHY-BE, paragraph "scaling factors for this activation
+             are integral power of 2"]. With amax = f * 2**e, f in [0.5, 1):
+             448 = 0.875 * 2**9, so p = e - 9 when f <= 0.875, else e - 8.
+    """
+    amax = np.asarray(amax, dtype=np.float32)
+    if not pow2:
+        s = amax / np.float32(E4M3_MAX)  # IEEE float32 division
+        return np.maximum(s, F32_MIN_NORMAL).astype(np.float32)
+    f, e = np.frexp(amax)
+    p = e.astype(np.int64) - 9 + (f > np.float32(0.875)).astype(np.int64)
+    p = np.where(amax == 0, -126, p)
+    p = np.maximum(p, -126)
+    return np.ldexp(np.float32(1.0), p).astype(np.float32)
+
+
+def _quantize_with_scale(x: np.ndarray, s: np.ndarray) -> np.ndarray:
+    """codes = enc(RN32(x / s)) (float32 division, correctly rounded)."""
+    return e4m3_encode(np.asarray(x, np.float32) / np.asarray(s, np.float32))
+
+
+# ---------------------------------------------------------------------------
+# Quantizers
+# ---------------------------------------------------------------------------
+def quant_act_1x128(x, pow2: bool = False):
+    """1x128 activation quantization [WHY-BE; OMG, paragraph on grouping].
+
+    x: float32 [M][K] (bf16 values widened exactly), K % 128 == 0.
+    Each (row m, K-block kb) tile of 128 contiguous elements gets its own
+    scale. Returns (codes uint8 [M][K], sa float32 [K/128][M]).
+    """
+    x = np.asarray(x, dtype=np.float32)
+    M, K = x.shape
+    assert K % TILE == 0
+    t = x.reshape(M, K // TILE, TILE)
+    s = tile_scale(np.abs(t).max(axis=2, initial=0.0), pow2)  # [M][KB]
+    q = _quantize_with_scale(t, s[:, :, None]).reshape(M, K)
+    return q, np.ascontiguousarray(s.T)
+
+
+def quant_act_1x128_transposed_input(xt, pow2: bool = False):
+    """Same tiles as quant_act_1x128 for the logical matrix X = xt^T, given
+    the input stored as xt [K][M] (tiles run down the rows of xt, i.e. they
+    are 128x1 tiles of the stored array). This is how the output gradient of
+    a Linear, stored token-major, is tiled along tokens for Wgrad [WHY-BE,
+    paragraph on 1x128 -> 128x1 tiles in the backward pass; OMG, Figure 6].
+    Returns (codes uint8 [M][K], s float32 [K/128][M]).
+    """
+    return quant_act_1x128(np.asarray(xt, dtype=np.float32).T, pow2)
+
+
+def quant_w_128x128(w, pow2: bool = False):
+    """128x128 weight-block quantization [WHY-BE].
+
+    w: float32 [K][N] (input-channel major, as a Linear weight is applied
+    y = x w), K % 128 == N % 128 == 0. One scale per 128x128 block.
+    Returns (codes uint8 [N][K], i.e. K-major, and sb float32 [K/128][N/128]).
+    """
+    w = np.asarray(w, dtype=np.float32)
+    K, N = w.shape
+    assert K % TILE == 0 and N % TILE == 0
+    b = w.reshape(K // TILE, TILE, N // TILE, TILE)
+    s = tile_scale(np.abs(b).max(axis=(1, 3), initial=0.0), pow2)  # [KB][NB]
+    q_kn = _quantize_with_scale(b, s[:, None, :, None]).reshape(K, N)
+    return np.ascontiguousarray(q_kn.T), s
+
+
+def dequant_act_1x128(q, sa) -> np.ndarray:
+    """RN32(dec(q) * s) for 1x128-tiled codes q [M][K], sa [K/128][M]."""
+    q = np.asarray(q, np.uint8)
+    M, K = q.shape
+    s = np.repeat(np.asarray(sa, np.float32).T, TILE, axis=1)  # [M][K]
+    return (e4m3_decode(q) * s.astype(np.float64)).astype(np.float32)
+
+
+def dequant_w_128x128(q, sb) -> np.ndarray:
+    """RN32(dec(q) * s) for K-major weight codes q [N][K], sb [K/128][N/128];
+    returned as [N][K]."""
+    q = np.asarray(q, np.uint8)
+    s = np.repeat(np.repeat(np.asarray(sb, np.float32).T, TILE, 0), TILE, 1)
+    return (e4m3_decode(q) * s.astype(np.float64)).astype(np.float32)
+
+
+def requant_1x128_to_128x1(q_in, s_in, pow2: bool = False):
+    """Backward-pass re-tiling of a cached FP8 activation [WHY-BE, paragraph
+    on 1x128 -> 128x1 tiles; paragraph on caching activations in FP8].
+
+    q_in: codes [T][C] with 1x128 tiles along C, s_in [C/128][T].
+    Dequantize exactly as x' = RN32(dec(q) * s_row), then quantize x' with
+    128x1 tiles (128 tokens of one channel), emitted transposed so that the
+    contraction over tokens is contiguous.
+    Returns (codes uint8 [C][T], s float32 [T/128][C]).
+    """
+    xprime = dequant_act_1x128(q_in, s_in)  # [T][C]
+    return quant_act_1x128(xprime.T, pow2)
+
+
+# ---------------------------------------------------------------------------
+# Block-scaled GEMM with promotion every 128 K
+# ---------------------------------------------------------------------------
+def gemm_blockscaled(qa, sa, qb, sb, scale_b: str = "128x128") -> np.ndarray:
+    """D[m][n] = sum over K-blocks kb of P_kb[m][n] * (sa[kb][m] * sbv[kb][n]),
+    P_kb = sum_{k in kb} dec(qa[m][k]) * dec(qb[n][k]), returned in float64.
+
+    Each 128-element chunk of K is summed on its own and then promoted: scaled
+    by the product of its A-tile and B-block scales and added to a high
+    precision accumulator [OMG, paragraph on promotion to FP32 registers on
+    CUDA cores with dequantization at promotion; FOOLED, Figure 7 (b)].
+
+    In float64 the chunk sum is exact: every E4M3 value is a multiple of 2**-9
+    and at most 448 in magnitude, so each product is a multiple of 2**-18 below
+    2**18 and a 128-term sum needs at most 43 significant bits. The library
+    matmul may therefore add in any order. sa*sb is exact too (24+24 bits).
+    The result is independent of where promotion happens, so it is also the
+    reference for the no-promotion variant.
+
+    qa [M][K], sa [K/128][M]; qb [N][K] (K-major);
+    scale_b "128x128": sb [K/128][ceil(N/128)], column n uses sb[kb][n // 128];
+    scale_b "1x128":   sb [K/128][N], column n uses sb[kb][n].
+    """
+    qa = np.asarray(qa, np.uint8)
+    qb = np.asarray(qb, np.uint8)
+    M, K = qa.shape
+    N, K2 = qb.shape
+    assert K == K2 and K % TILE == 0
+    A = e4m3_decode(qa)
+    B = e4m3_decode(qb)
+    sa = np.asarray(sa, np.float32).astype(np.float64)
+    sb = np.asarray(sb, np.float32).astype(np.float64)
+    out = np.zeros((M, N), dtype=np.float64)
+    for kb in range(K // TILE):
+        ks = slice(kb * TILE, (kb + 1) * TILE)
+        P = A[:, ks] @ B[:, ks].T  # exact chunk sum
+        if scale_b == "128x128":
+            sbv = sb[kb][np.arange(N) // TILE]
+        elif scale_b == "1x128":
+            sbv = sb[kb]
+        else:
+            raise ValueError(scale_b)
+        out += P * (sa[kb][:, None] * sbv[None, :])
+    return out
+
+
+def grouped_gemm_blockscaled(qa, sa, m_offsets, qb, sb) -> np.ndarray:
+    """MoE up-projection on expert-sorted rows [HEARAON, paragraph on FP8
+    quantization before MoE up-projection and dispatch; OMG, same paragraph].
+
+    qa [Mtot][K] with rows of expert e in m_offsets[e] .. m_offsets[e+1];
+    sa [K/128][Mtot]; qb [E][N][K]; sb [E][K/128][N/128].
+    Each segment is the dense block-scaled GEMM against its own expert.
+    """
+    qa = np.asarray(qa, np.uint8)
+    offs = [int(v) for v in m_offsets]
+    E = len(offs) - 1
+    N = qb.shape[1]
+    out = np.zeros((qa.shape[0], N), dtype=np.float64)
+    for e in range(E):
+        r0, r1 = offs[e], offs[e + 1]
+        if r1 > r0:
+            out[r0:r1] = gemm_blockscaled(qa[r0:r1], np.asarray(sa)[:, r0:r1],
+                                          qb[e], sb[e])
+    return out
+
+
+# ---------------------------------------------------------------------------
+# Error measures for the accumulation study
+# ---------------------------------------------------------------------------
+def row_col_norms(qa, sa, qb, sb, scale_b: str = "128x128"):
+    """||a_i||_2 and ||b_j||_2 of the dequantized operands, float64."""
+    a = e4m3_decode(qa) * np.repeat(np.asarray(sa, np.float64).T, TILE, 1)
+    sbf = np.asarray(sb, np.float64)
+    if scale_b == "128x128":
+        sbe = np.repeat(sbf.T, TILE, 0)[: qb.shape[0]]  # [N][KB]
+    else:
+        sbe = sbf.T
+    b = e4m3_decode(qb) * np.repeat(sbe, TILE, 1)
+    return np.sqrt((a * a).sum(1)), np.sqrt((b * b).sum(1))
+
+
+def max_relative_error(c, r) -> float:
+    """max|C - R| / max|R| ([WHY-BE] quotes ~2% of this kind at K = 4096 for
+    tensor-core-only accumulation on Hopper; the page does not define it, this
+    is one of the two measures reported)."""
+    c = np.asarray(c, np.float64)
+    r = np.asarray(r, np.float64)
+    return float(np.abs(c - r).max() / max(np.abs(r).max(), 1e-300))

@@ -1,0 +1,397 @@
+"""Pins for the CPU oracle (no GPU).
+
+Each check ties the oracle to something other than itself: exhaustive exact
+search over the E4M3 code space, a float8 library cast, hand-worked values in
+tests/golden, closed forms, exact-integer GEMMs against int64 matmul and exact
+rational brute force on tiny inputs. The planted-mistake tests at the end show
+that plausible slips in the oracle fail these pins.
+"""
+from __future__ import annotations
+
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+import oracle.fp8q_oracle as O
+from tests import bruteforce as BF
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _parse_float(tok: str) -> float:
+    return float.fromhex(tok) if "0x" in tok.lower() and "p" in tok.lower() else float(tok)
+
+
+# ---------------------------------------------------------------------------
+# pin functions (reused by the planted-mistake tests)
+# ---------------------------------------------------------------------------
+def pin_decode_all_codes():
+    codes = np.arange(256, dtype=np.uint8)
+    got = O.e4m3_decode(codes)
+    lib = torch.from_numpy(codes.copy()).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    for c in range(256):
+        exact = BF.e4m3_value(c)
+        if exact is None:
+            assert math.isnan(got[c]) and math.isnan(lib[c]), hex(c)
+        else:
+            assert got[c] == float(exact) == lib[c], hex(c)
+            assert math.copysign(1, got[c]) == math.copysign(1, lib[c]), hex(c)
+
+
+def pin_encode_roundtrip_and_midpoints():
+    finite = [c for c in range(256) if c & 0x7F != 0x7F]
+    vals = np.array([float(BF.e4m3_value(c)) for c in finite], dtype=np.float32)
+    vals[finite.index(0x80)] = -0.0
+    assert (O.e4m3_encode(vals) == np.array(finite, np.uint8)).all()
+    # every midpoint between neighbouring same-sign magnitudes goes to the even code
+    mids, want = [], []
+    for c in range(126):
+        lo, hi = BF.e4m3_value(c), BF.e4m3_value(c + 1)
+        m = (lo + hi) / 2
+        even = c if c % 2 == 0 else c + 1
+        mids += [float(m), -float(m)]
+        want += [even, even | 0x80]
+    assert (O.e4m3_encode(np.array(mids, np.float32)) == np.array(want, np.uint8)).all()
+
+
+def pin_encode_bruteforce(seed=0, n=3000):
+    rng = np.random.default_rng(seed)
+    # magnitudes spread over 2^-14 .. 2^10 (subnormal, normal and saturating ranges)
+    v = (rng.standard_normal(n) * np.exp2(rng.uniform(-14, 10, n))).astype(np.float32)
+    # plus values one float32 ulp either side of every midpoint
+    mids = []
+    for c in range(126):
+        m = np.float32(float((BF.e4m3_value(c) + BF.e4m3_value(c + 1)) / 2))
+        mids += [np.nextafter(m, np.float32(0)), np.nextafter(m, np.float32(1e9))]
+    v = np.concatenate([v, np.array(mids, np.float32), -np.array(mids, np.float32)])
+    got = O.e4m3_encode(v)
+    want = np.array([BF.encode(float(x)) for x in v], np.uint8)
+    assert (got == want).all()
+
+
+def pin_encode_library_cast(seed=1, n=200000):
+    rng = np.random.default_rng(seed)
+    v = (rng.standard_normal(n) * np.exp2(rng.uniform(-12, 8.7, n))).astype(np.float32)
+    v = v[np.abs(v) <= 448]
+    lib = torch.from_numpy(v).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert (O.e4m3_encode(v) == lib).all()
+
+
+def pin_golden_encodings():
+    rows = []
+    with open(os.path.join(GOLDEN, "e4m3_worked_values.txt")) as f:
+        for line in f:
+            line = line.split("#")[0].strip()
+            if line:
+                a, b = line.split()[:2]
+                rows.append((_parse_float(a), int(b, 16)))
+    v = np.array([r[0] for r in rows], np.float32)
+    assert [int(c) for c in O.e4m3_encode(v)] == [r[1] for r in rows]
+
+
+def pin_golden_tile():
+    with open(os.path.join(GOLDEN, "tile_1x128_handworked.txt")) as f:
+        lines = [l.split("#")[0].strip() for l in f]
+    lines = [l for l in lines if l]
+    scale = float.fromhex(lines[0].split()[1])
+    entries = [l.split() for l in lines[2:]]
+    x = np.zeros((1, 128), np.float32)
+    for idx, val, _ in entries:
+        x[0, int(idx)] = float(val)
+    for pow2 in (False, True):
+        q, s = O.quant_act_1x128(x, pow2)
+        assert s.shape == (1, 1) and s[0, 0] == np.float32(scale)
+        for idx, _, code in entries:
+            assert q[0, int(idx)] == int(code, 16)
+        assert (q[0, 5:] == 0).all()
+
+
+def pin_scale_closed_forms():
+    # amax = 448 * 2^j gives s = 2^j in both modes
+    j = np.arange(-120, 100)
+    amax = (448.0 * np.exp2(j.astype(np.float64))).astype(np.float32)
+    for pow2 in (False, True):
+        assert (O.tile_scale(amax, pow2) == np.exp2(j).astype(np.float32)).all()
+    # all-zero tile -> 2^-126 in both modes
+    for pow2 in (False, True):
+        assert O.tile_scale(np.float32(0), pow2) == np.float32(2.0 ** -126)
+    # power-of-two ceiling invariant: amax/s <= 448 < 2*amax/s
+    rng = np.random.default_rng(3)
+    a = (rng.uniform(0.5, 1, 5000) * np.exp2(rng.integers(-100, 100, 5000))).astype(np.float32)
+    s = O.tile_scale(a, True).astype(np.float64)
+    a = a.astype(np.float64)
+    assert (a / s <= 448).all() and (2 * a / s > 448).all()
+
+
+def pin_scale_bruteforce(seed=4, n=400):
+    rng = np.random.default_rng(seed)
+    a = (rng.uniform(0.5, 1, n) * np.exp2(rng.integers(-140, 120, n))).astype(np.float32)
+    a = np.concatenate([a, np.float32([448.0 * 2.0 ** k for k in (-3, 0, 5)]),
+                        np.float32([1e-45, 3.5, 448.0, 449.0, 447.99997])])
+    for pow2 in (False, True):
+        got = O.tile_scale(a, pow2)
+        for x, g in zip(a, got):
+            assert Fraction(float(g)) == BF.scale_of(Fraction(float(x)), pow2), (x, pow2)
+
+
+def _bf16_tensor(shape, seed, std=1.0, outliers=0):
+    g = torch.Generator().manual_seed(seed)
+    x = torch.randn(shape, generator=g) * std
+    if outliers:
+        idx = torch.randperm(x.numel(), generator=g)[:outliers]
+        x.view(-1)[idx] *= 100.0
+    return x.to(torch.bfloat16).float().numpy()
+
+
+def pin_quant_act_bruteforce(pow2):
+    x = _bf16_tensor((3, 256), seed=5, outliers=4)
+    x[1, 128:] = 0.0              # an all-zero tile
+    x[2, :128] *= 1e-38           # a tile of float32 subnormals
+    x[0, 3] = -0.0
+    q, sa = O.quant_act_1x128(x, pow2)
+    assert q.shape == (3, 256) and sa.shape == (2, 3)
+    for m in range(3):
+        for kb in range(2):
+            codes, s = BF.quant_tile([float(v) for v in x[m, kb * 128:(kb + 1) * 128]], pow2)
+            assert Fraction(float(sa[kb, m])) == s
+            assert list(q[m, kb * 128:(kb + 1) * 128]) == codes
+
+
+def pin_quant_w_bruteforce(pow2):
+    w = _bf16_tensor((256, 128), seed=6, std=0.02, outliers=2)
+    q, sb = O.quant_w_128x128(w, pow2)
+    assert q.shape == (128, 256) and sb.shape == (2, 1)
+    for kb in range(2):
+        blk = w[kb * 128:(kb + 1) * 128, :]
+        codes, s = BF.quant_tile([float(v) for v in blk.reshape(-1)], pow2)
+        assert Fraction(float(sb[kb, 0])) == s
+        codes = np.array(codes, np.uint8).reshape(128, 128)  # [k][n]
+        assert (q[:, kb * 128:(kb + 1) * 128] == codes.T).all()
+
+
+def pin_quant_transposed_bruteforce():
+    xt = _bf16_tensor((256, 3), seed=7)  # stored [K][M]
+    q, s = O.quant_act_1x128_transposed_input(xt, False)
+    assert q.shape == (3, 256) and s.shape == (2, 3)
+    for m in range(3):
+        for kb in range(2):
+            codes, sc = BF.quant_tile([float(v) for v in xt[kb * 128:(kb + 1) * 128, m]], False)
+            assert Fraction(float(s[kb, m])) == sc
+            assert list(q[m, kb * 128:(kb + 1) * 128]) == codes
+
+
+def pin_requant_bruteforce(pow2):
+    x = _bf16_tensor((128, 256), seed=8, outliers=3)  # [T][C]
+    q_in, s_in = O.quant_act_1x128(x, pow2)
+    q_out, s_out = O.requant_1x128_to_128x1(q_in, s_in, pow2)
+    assert q_out.shape == (256, 128) and s_out.shape == (1, 256)
+    for c in range(0, 256, 5):
+        xs = [float(BF.round_to_f32(BF.e4m3_value(int(q_in[t, c])) *
+                                    Fraction(float(s_in[c // 128, t])))) for t in range(128)]
+        codes, s = BF.quant_tile(xs, pow2)
+        assert Fraction(float(s_out[0, c])) == s
+        assert list(q_out[c, :]) == codes
+
+
+def pin_requant_identity():
+    # every 1x128 row tile and every 128x1 column tile holds a 448 -> all scales 1 and
+    # codes pass through unchanged (transposed), in both scale modes
+    rng = np.random.default_rng(9)
+    T, C = 256, 256
+    codes = rng.integers(0, 0x7E, (T, C)).astype(np.uint8)
+    codes[codes & 0x7F == 0x7F] = 0
+    for t in range(T):
+        codes[t, (t % 128)] = 0x7E
+        codes[t, 128 + (t % 128)] = 0xFE
+    s_in = np.ones((C // 128, T), np.float32)
+    for pow2 in (False, True):
+        q_out, s_out = O.requant_1x128_to_128x1(codes, s_in, pow2)
+        assert (s_out == 1).all()
+        assert (q_out == codes.T).all()
+
+
+def pin_gemm_exact_integer():
+    # integer entries |v| <= 16 are exact in E4M3; one +-448 per tile forces s = 1
+    rng = np.random.default_rng(10)
+    M, N, K = 37, 256, 384
+    A = rng.integers(-16, 17, (M, K)).astype(np.float32)
+    W = rng.integers(-16, 17, (K, N)).astype(np.float32)
+    for kb in range(K // 128):
+        A[:, kb * 128 + rng.integers(0, 128)] = 448.0
+        for nb in range(N // 128):
+            W[kb * 128 + 5, nb * 128 + 7] = -448.0
+    qa, sa = O.quant_act_1x128(A, False)
+    qb, sb = O.quant_w_128x128(W, False)
+    assert (sa == 1).all() and (sb == 1).all()
+    got = O.gemm_blockscaled(qa, sa, qb, sb)
+    want = A.astype(np.int64) @ W.astype(np.int64)
+    assert (got == want).all()
+
+
+def pin_gemm_rank1_closed_form():
+    # constant codes per (row, K-block) and per (column, K-block):
+    # D[i][j] = sum_kb 128 * dec(ca[i,kb]) * dec(cb[j,kb]) * sa[kb][i] * sbv[kb][j]
+    rng = np.random.default_rng(11)
+    M, N, KB = 5, 384, 3
+    ca = rng.integers(1, 0x7E, (M, KB)).astype(np.uint8)
+    cb = rng.integers(0x81, 0xFE, (N, KB)).astype(np.uint8)
+    qa = np.repeat(ca, 128, axis=1)
+    qb = np.repeat(cb, 128, axis=1)
+    sa = np.exp2(rng.integers(-8, 8, (KB, M))).astype(np.float32)
+    for mode in ("128x128", "1x128"):
+        nsb = N // 128 if mode == "128x128" else N
+        sb = (rng.uniform(0.5, 2, (KB, nsb)) * 2.0 ** -5).astype(np.float32)
+        got = O.gemm_blockscaled(qa, sa, qb, sb, mode)
+        da = np.array([[float(BF.e4m3_value(int(c))) for c in r] for r in ca])
+        db = np.array([[float(BF.e4m3_value(int(c))) for c in r] for r in cb])
+        want = np.zeros((M, N))
+        for kb in range(KB):
+            sbv = sb[kb][np.arange(N) // 128] if mode == "128x128" else sb[kb]
+            want += 128 * np.outer(da[:, kb] * sa[kb], db[:, kb] * sbv)
+        assert np.allclose(got, want, rtol=1e-14, atol=0)
+
+
+def pin_gemm_bruteforce():
+    rng = np.random.default_rng(12)
+    M, N, K = 2, 257, 256   # N spans two 128-column blocks and one extra column
+    qa = rng.integers(0, 256, (M, K)).astype(np.uint8)
+    qb = rng.integers(0, 256, (N, K)).astype(np.uint8)
+    qa[(qa & 0x7F) == 0x7F] = 0x11
+    qb[(qb & 0x7F) == 0x7F] = 0x22
+    sa = rng.uniform(1e-3, 1, (K // 128, M)).astype(np.float32)
+    for mode in ("128x128", "1x128"):
+        nsb = -(-N // 128) if mode == "128x128" else N
+        sb = rng.uniform(1e-3, 1, (K // 128, nsb)).astype(np.float32)
+        got = O.gemm_blockscaled(qa, sa, qb, sb, mode)
+        exact, mag = BF.gemm_exact(qa.tolist(), sa, qb.tolist(), sb, mode)
+        for i in range(M):
+            for j in range(N):
+                # exact chunk sums; the only roundings are the promotion product and
+                # the float64 sum over two chunks: a few ulps of the summed magnitudes
+                assert abs(Fraction(float(got[i, j])) - exact[i][j]) <= mag[i][j] * Fraction(1, 2 ** 50)
+
+
+def pin_grouped_segments():
+    rng = np.random.default_rng(13)
+    E, N, K = 4, 128, 256
+    offs = [0, 3, 3, 4, 9]          # one empty expert, one 1-row expert
+    Mtot = offs[-1]
+    qa = rng.integers(0, 0x7E, (Mtot, K)).astype(np.uint8)
+    qb = rng.integers(0, 0x7E, (E, N, K)).astype(np.uint8)
+    sa = rng.uniform(0.1, 1, (K // 128, Mtot)).astype(np.float32)
+    sb = rng.uniform(0.1, 1, (E, K // 128, N // 128)).astype(np.float32)
+    got = O.grouped_gemm_blockscaled(qa, sa, offs, qb, sb)
+    for r in range(Mtot):
+        e = max(i for i in range(E) if offs[i] <= r)
+        for j in (0, 77, 127):
+            p = 0.0
+            for kb in range(K // 128):
+                chunk = sum(float(BF.e4m3_value(int(qa[r, k])) * BF.e4m3_value(int(qb[e, j, k])))
+                            for k in range(kb * 128, kb * 128 + 128))
+                p += chunk * float(sa[kb, r]) * float(sb[e, kb, j // 128])
+            assert abs(got[r, j] - p) <= 1e-12 * max(abs(p), 1e-30)
+
+
+def pin_norms_and_error_measure():
+    rng = np.random.default_rng(14)
+    qa = np.full((2, 128), 0x38, np.uint8)   # all ones
+    qb = np.full((3, 128), 0x40, np.uint8)   # all twos
+    sa = np.array([[1.0, 2.0]], np.float32)
+    sb = np.array([[0.5]], np.float32)
+    na, nb = O.row_col_norms(qa, sa, qb, sb)
+    assert np.allclose(na, [math.sqrt(128), 2 * math.sqrt(128)])
+    assert np.allclose(nb, [math.sqrt(128)] * 3)
+    r = rng.standard_normal((4, 4))
+    c = r.copy()
+    c[1, 2] += 0.01 * np.abs(r).max()
+    assert math.isclose(O.max_relative_error(c, r), 0.01, rel_tol=1e-9)
+
+
+ALL_PINS = [
+    pin_decode_all_codes, pin_encode_roundtrip_and_midpoints, pin_encode_bruteforce,
+    pin_encode_library_cast, pin_golden_encodings, pin_golden_tile, pin_scale_closed_forms,
+    pin_scale_bruteforce, lambda: pin_quant_act_bruteforce(False),
+    lambda: pin_quant_act_bruteforce(True), lambda: pin_quant_w_bruteforce(False),
+    lambda: pin_quant_w_bruteforce(True), pin_quant_transposed_bruteforce,
+    lambda: pin_requant_bruteforce(False), lambda: pin_requant_bruteforce(True),
+    pin_requant_identity, pin_gemm_exact_integer, pin_gemm_rank1_closed_form,
+    pin_gemm_bruteforce, pin_grouped_segments, pin_norms_and_error_measure,
+]
+
+
+@pytest.mark.parametrize("pin", ALL_PINS, ids=lambda f: getattr(f, "__name__", "pin"))
+def test_oracle_pin(pin):
+    pin()
+
+
+# ---------------------------------------------------------------------------
+# planted mistakes: each must be caught by at least one pin
+# ---------------------------------------------------------------------------
+def _fails(pins):
+    for p in pins:
+        try:
+            p()
+        except AssertionError:
+            return True
+    return False
+
+
+def test_planted_ties_away_from_zero(monkeypatch):
+    orig = O.e4m3_encode
+
+    def ties_away(v):
+        v = np.asarray(v, np.float32)
+        a = np.abs(v).astype(np.float64)
+        lo = np.clip(np.searchsorted(O._E4M3_NONNEG, a, side="right") - 1, 0, 126)
+        hi = np.minimum(lo + 1, 126)
+        mid = (O._E4M3_NONNEG[lo] + O._E4M3_NONNEG[hi]) / 2
+        code = np.where(a < mid, lo, hi)
+        return (code | np.where(np.signbit(v), 0x80, 0)).astype(np.uint8)
+
+    monkeypatch.setattr(O, "e4m3_encode", ties_away)
+    assert _fails([pin_encode_roundtrip_and_midpoints, pin_golden_encodings])
+    monkeypatch.setattr(O, "e4m3_encode", orig)
+
+
+def test_planted_pow2_threshold(monkeypatch):
+    real = O.tile_scale
+
+    def off_by_one(amax, pow2):
+        if not pow2:
+            return real(amax, pow2)
+        amax = np.asarray(amax, np.float32)
+        f, e = np.frexp(amax)
+        p = np.maximum(np.where(amax == 0, -126, e - 9 + (f >= 0.875)), -126)
+        return np.ldexp(np.float32(1), p).astype(np.float32)
+
+    monkeypatch.setattr(O, "tile_scale", off_by_one)
+    assert _fails([pin_scale_closed_forms, pin_scale_bruteforce])
+
+
+def test_planted_scale_index(monkeypatch):
+    real = O.gemm_blockscaled
+
+    def wrong_block_index(qa, sa, qb, sb, scale_b="128x128"):
+        if scale_b != "128x128":
+            return real(qa, sa, qb, sb, scale_b)
+        N = qb.shape[0]
+        sbw = np.asarray(sb)[:, (np.arange(N) % sb.shape[1])]  # n % NB instead of n // 128
+        return real(qa, sa, qb, sbw, "1x128")
+
+    monkeypatch.setattr(O, "gemm_blockscaled", wrong_block_index)
+    assert _fails([pin_gemm_rank1_closed_form, pin_gemm_bruteforce])
+
+
+def test_planted_reversed_token_scale(monkeypatch):
+    real = O.requant_1x128_to_128x1
+
+    def reversed_tokens(q_in, s_in, pow2=False):
+        # reads the row scale of token T-1-t instead of t: a plausible indexing slip
+        return real(q_in, np.ascontiguousarray(np.asarray(s_in)[:, ::-1]), pow2)
+
+    monkeypatch.setattr(O, "requant_1x128_to_128x1", reversed_tokens)
+    assert _fails([lambda: pin_requant_bruteforce(False)])
