@@ -1,0 +1,295 @@
+// C ABI of libfp8q.so (declared in include/fp8q.h): argument validation,
+// TMA tensor-map encoding, kernel selection and launch, device status.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "fp8q.h"
+#include "gemm.cuh"
+#include "ptx.cuh"
+#include "quant.cuh"
+
+#define FP8Q_API extern "C" __attribute__((visibility("default")))
+
+namespace {
+
+// One status word per device (a __device__ variable has a copy on every
+// device the module is loaded on). Kernels OR error bits into it.
+__device__ unsigned int g_device_status;
+
+constexpr int kMaxDevices = 64;
+constexpr uint64_t kWaitLimitNs = 4000000000ull;  // 4 s: far above any legal wait
+
+struct DeviceInfo {
+  bool ready = false;
+  bool supported = false;
+  bool gemm_ok = false;  // the GEMM's register split matches its compiled count
+  int num_sms = 0;
+  unsigned* status = nullptr;
+};
+
+std::mutex g_mutex;
+DeviceInfo g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+bool g_encode_tried = false;
+
+fp8q_status device_info(DeviceInfo** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FP8Q_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.ready) {
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return FP8Q_ERR_CUDA;
+    // the kernels are built for sm_103a only
+    d.supported = (prop.major == 10 && prop.minor == 3);
+    d.num_sms = prop.multiProcessorCount;
+    if (d.supported) {
+      const int smem = static_cast<int>(fp8q::gemm::Layout::bytes(fp8q::gemm::kMaxExperts));
+      if (cudaFuncSetAttribute(fp8q::gemm::gemm_blockscaled_kernel,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+        return FP8Q_ERR_CUDA;
+      // setmaxnreg.inc can only hand out what the block was launched with: a
+      // split that exceeds it would wait forever, so check before any launch.
+      cudaFuncAttributes fa;
+      if (cudaFuncGetAttributes(&fa, fp8q::gemm::gemm_blockscaled_kernel) != cudaSuccess)
+        return FP8Q_ERR_CUDA;
+      d.gemm_ok = fa.numRegs == fp8q::gemm::kLaunchRegs &&
+                  fa.maxThreadsPerBlock >= fp8q::gemm::kThreads;
+      void* addr = nullptr;
+      if (cudaGetSymbolAddress(&addr, g_device_status) != cudaSuccess) return FP8Q_ERR_CUDA;
+      d.status = static_cast<unsigned*>(addr);
+    }
+    if (!g_encode_tried) {
+      g_encode_tried = true;
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                           cudaEnableDefault, &q) == cudaSuccess &&
+          q == cudaDriverEntryPointSuccess)
+        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    d.ready = true;
+  }
+  if (!d.supported) return FP8Q_ERR_UNSUPPORTED;
+  if (!g_encode) return FP8Q_ERR_CUDA;
+  *out = &d;
+  return FP8Q_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+fp8q_status launch_status() {
+  return cudaGetLastError() == cudaSuccess ? FP8Q_OK : FP8Q_ERR_CUDA;
+}
+
+// 2D uint8 tensor map [outer][inner] (row stride row_bytes), box
+// box_inner x box_outer, 128-byte swizzle, zero fill out of bounds.
+bool encode_u8_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                  uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool env_flag(const char* name) {
+  const char* v = std::getenv(name);
+  return v && v[0] && std::strcmp(v, "0") != 0;
+}
+
+fp8q_status gemm_common(const uint8_t* A, const float* sa, const int32_t* m_offsets, int E,
+                        const uint8_t* B, const float* sb, int64_t M, int64_t N, int64_t K,
+                        void* D, int64_t ldd, unsigned flags, cudaStream_t stream) {
+  using namespace fp8q::gemm;
+  const bool grouped = m_offsets != nullptr;
+  const unsigned allowed = grouped ? (FP8Q_OUT_BF16 | FP8Q_NO_PROMOTION)
+                                   : (FP8Q_OUT_BF16 | FP8Q_NO_PROMOTION | FP8Q_SCALE_B_1x128);
+  if (flags & ~allowed) return FP8Q_ERR_INVALID_ARG;
+  if (M < 0 || N <= 0 || K <= 0 || N % 128 || K % 128) return FP8Q_ERR_SHAPE;
+  if (ldd < N) return FP8Q_ERR_SHAPE;
+  if (E < 1 || E > kMaxExperts) return FP8Q_ERR_SHAPE;
+  // TMA coordinates and tile counts are 32-bit
+  if (M >= (1ll << 31) || K >= (1ll << 31) || static_cast<int64_t>(E) * N >= (1ll << 31))
+    return FP8Q_ERR_SHAPE;
+  if (M == 0) return FP8Q_OK;
+  if (!A || !sa || !B || !sb || !D) return FP8Q_ERR_INVALID_ARG;
+  const int out_bytes = (flags & FP8Q_OUT_BF16) ? 2 : 4;
+  if (!aligned16(A) || !aligned16(B) || !aligned16(D) || !aligned4(sa) || !aligned4(sb) ||
+      (ldd * out_bytes) % 16)
+    return FP8Q_ERR_ALIGN;
+  if ((flags & FP8Q_SCALE_B_1x128) && !aligned16(sb)) return FP8Q_ERR_ALIGN;
+
+  DeviceInfo* dev = nullptr;
+  if (fp8q_status st = device_info(&dev)) return st;
+  if (!dev->gemm_ok) return FP8Q_ERR_UNSUPPORTED;
+
+  const uint32_t box_a_rows = static_cast<uint32_t>(M < BM ? M : BM);
+  const int64_t b_rows = static_cast<int64_t>(E) * N;
+  const uint32_t box_b_rows = static_cast<uint32_t>(b_rows < BN ? b_rows : BN);
+  CUtensorMap tmA, tmB;
+  if (!encode_u8_2d(&tmA, A, K, M, K, BK, box_a_rows)) return FP8Q_ERR_CUDA;
+  if (!encode_u8_2d(&tmB, B, K, b_rows, K, BK, box_b_rows)) return FP8Q_ERR_CUDA;
+
+  Params p;
+  p.sa = sa;
+  p.sb = sb;
+  p.D = D;
+  p.m_offsets = m_offsets;
+  p.status = dev->status;
+  p.M = M;
+  p.ldd = ldd;
+  p.N = static_cast<int>(N);
+  p.K = static_cast<int>(K);
+  p.E = E;
+  p.flags = ((flags & FP8Q_NO_PROMOTION) ? 0 : kFlagPromote) |
+            ((flags & FP8Q_OUT_BF16) ? kFlagOutBF16 : 0) |
+            ((flags & FP8Q_SCALE_B_1x128) ? kFlagScaleB1x128 : 0);
+  p.group_m = 16;
+  p.tx_bytes = (box_a_rows + box_b_rows) * BK;
+  p.inject_timeout = env_flag("FP8Q_DEBUG_INJECT_TIMEOUT") ? 1 : 0;
+  p.wait_limit_ns = kWaitLimitNs;
+
+  int grid = dev->num_sms;
+  if (!grouped) {
+    const int64_t tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+    if (tiles < grid) grid = static_cast<int>(tiles);
+  }
+  const size_t smem = Layout::bytes(E);
+  gemm_blockscaled_kernel<<<grid, kThreads, smem, stream>>>(tmA, tmB, p);
+  return launch_status();
+}
+
+}  // namespace
+
+FP8Q_API fp8q_status fp8q_quant_act_1x128(const void* x, int64_t M, int64_t K, int64_t ldx,
+                                          uint8_t* q, int64_t ldq, float* sa, unsigned flags,
+                                          fp8q_stream_t stream) {
+  if (flags & ~static_cast<unsigned>(FP8Q_POW2_SCALE | FP8Q_TRANSPOSED_INPUT))
+    return FP8Q_ERR_INVALID_ARG;
+  const bool transposed = flags & FP8Q_TRANSPOSED_INPUT;
+  const bool pow2 = flags & FP8Q_POW2_SCALE;
+  if (M < 0 || K <= 0 || K % 128) return FP8Q_ERR_SHAPE;
+  if (ldq < K || ldx < (transposed ? M : K)) return FP8Q_ERR_SHAPE;
+  if (K / 128 > 65535 || M >= (1ll << 40)) return FP8Q_ERR_SHAPE;
+  if (M == 0) return FP8Q_OK;
+  if (!x || !q || !sa) return FP8Q_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(q) || !aligned4(sa) || (ldx * 2) % 16 || ldq % 16)
+    return FP8Q_ERR_ALIGN;
+  DeviceInfo* dev = nullptr;
+  if (fp8q_status st = device_info(&dev)) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const auto* xb = static_cast<const __nv_bfloat16*>(x);
+  if (!transposed) {
+    const dim3 grid(static_cast<unsigned>((M + fp8q::kRowQuantRows - 1) / fp8q::kRowQuantRows),
+                    static_cast<unsigned>(K / 128));
+    if (pow2)
+      fp8q::quant_rows_1x128_kernel<true><<<grid, 256, 0, s>>>(xb, M, ldx, q, ldq, sa);
+    else
+      fp8q::quant_rows_1x128_kernel<false><<<grid, 256, 0, s>>>(xb, M, ldx, q, ldq, sa);
+  } else {
+    // stored [K][M]: R = K rows, Cc = M columns, 128x1 column tiles
+    const dim3 grid(static_cast<unsigned>((M + 127) / 128), static_cast<unsigned>(K / 128));
+    if (pow2)
+      fp8q::quant_cols_kernel<0, false, true><<<grid, 256, 0, s>>>(x, K, M, ldx, nullptr, q, ldq, sa);
+    else
+      fp8q::quant_cols_kernel<0, false, false><<<grid, 256, 0, s>>>(x, K, M, ldx, nullptr, q, ldq, sa);
+  }
+  return launch_status();
+}
+
+FP8Q_API fp8q_status fp8q_quant_w_128x128(const void* w, int64_t K, int64_t N, uint8_t* q,
+                                          float* sb, unsigned flags, fp8q_stream_t stream) {
+  if (flags & ~static_cast<unsigned>(FP8Q_POW2_SCALE)) return FP8Q_ERR_INVALID_ARG;
+  if (K <= 0 || N <= 0 || K % 128 || N % 128) return FP8Q_ERR_SHAPE;
+  if (K / 128 > 65535) return FP8Q_ERR_SHAPE;
+  if (!w || !q || !sb) return FP8Q_ERR_INVALID_ARG;
+  if (!aligned16(w) || !aligned16(q) || !aligned4(sb)) return FP8Q_ERR_ALIGN;
+  DeviceInfo* dev = nullptr;
+  if (fp8q_status st = device_info(&dev)) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const dim3 grid(static_cast<unsigned>(N / 128), static_cast<unsigned>(K / 128));
+  if (flags & FP8Q_POW2_SCALE)
+    fp8q::quant_cols_kernel<0, true, true><<<grid, 256, 0, s>>>(w, K, N, N, nullptr, q, K, sb);
+  else
+    fp8q::quant_cols_kernel<0, true, false><<<grid, 256, 0, s>>>(w, K, N, N, nullptr, q, K, sb);
+  return launch_status();
+}
+
+FP8Q_API fp8q_status fp8q_requant_1x128_to_128x1(const uint8_t* q_in, const float* s_in,
+                                                 int64_t T, int64_t C, uint8_t* q_out,
+                                                 float* s_out, unsigned flags,
+                                                 fp8q_stream_t stream) {
+  if (flags & ~static_cast<unsigned>(FP8Q_POW2_SCALE)) return FP8Q_ERR_INVALID_ARG;
+  if (T <= 0 || C <= 0 || T % 128 || C % 128) return FP8Q_ERR_SHAPE;
+  if (T / 128 > 65535) return FP8Q_ERR_SHAPE;
+  if (!q_in || !s_in || !q_out || !s_out) return FP8Q_ERR_INVALID_ARG;
+  if (!aligned16(q_in) || !aligned16(q_out) || !aligned4(s_in) || !aligned4(s_out))
+    return FP8Q_ERR_ALIGN;
+  DeviceInfo* dev = nullptr;
+  if (fp8q_status st = device_info(&dev)) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const dim3 grid(static_cast<unsigned>(C / 128), static_cast<unsigned>(T / 128));
+  if (flags & FP8Q_POW2_SCALE)
+    fp8q::quant_cols_kernel<1, false, true><<<grid, 256, 0, s>>>(q_in, T, C, C, s_in, q_out, T, s_out);
+  else
+    fp8q::quant_cols_kernel<1, false, false><<<grid, 256, 0, s>>>(q_in, T, C, C, s_in, q_out, T, s_out);
+  return launch_status();
+}
+
+FP8Q_API fp8q_status fp8q_gemm_blockscaled(const uint8_t* A, const float* sa, const uint8_t* B,
+                                           const float* sb, int64_t M, int64_t N, int64_t K,
+                                           void* D, int64_t ldd, unsigned flags,
+                                           fp8q_stream_t stream) {
+  return gemm_common(A, sa, nullptr, 1, B, sb, M, N, K, D, ldd, flags,
+                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+FP8Q_API fp8q_status fp8q_grouped_gemm(const uint8_t* A, const float* sa,
+                                       const int32_t* m_offsets, int E, const uint8_t* B,
+                                       const float* sb, int64_t Mtot, int64_t N, int64_t K,
+                                       void* D, unsigned flags, fp8q_stream_t stream) {
+  if (!m_offsets) return FP8Q_ERR_INVALID_ARG;
+  return gemm_common(A, sa, m_offsets, E, B, sb, Mtot, N, K, D, N, flags,
+                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+FP8Q_API fp8q_status fp8q_get_status(fp8q_stream_t stream) {
+  DeviceInfo* dev = nullptr;
+  if (fp8q_status st = device_info(&dev)) return st;
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return FP8Q_ERR_CUDA;
+  unsigned v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_device_status, sizeof(v)) != cudaSuccess) return FP8Q_ERR_CUDA;
+  if (v) {
+    const unsigned zero = 0;
+    if (cudaMemcpyToSymbol(g_device_status, &zero, sizeof(zero)) != cudaSuccess)
+      return FP8Q_ERR_CUDA;
+  }
+  if (v & fp8q::kDevStatusTimeout) return FP8Q_ERR_TIMEOUT;
+  if (v & fp8q::kDevStatusBadOffsets) return FP8Q_ERR_INVALID_ARG;
+  return FP8Q_OK;
+}
+
+FP8Q_API const char* fp8q_status_string(fp8q_status status) {
+  switch (status) {
+    case FP8Q_OK: return "FP8Q_OK";
+    case FP8Q_ERR_INVALID_ARG: return "FP8Q_ERR_INVALID_ARG";
+    case FP8Q_ERR_SHAPE: return "FP8Q_ERR_SHAPE";
+    case FP8Q_ERR_ALIGN: return "FP8Q_ERR_ALIGN";
+    case FP8Q_ERR_UNSUPPORTED: return "FP8Q_ERR_UNSUPPORTED";
+    case FP8Q_ERR_CUDA: return "FP8Q_ERR_CUDA";
+    case FP8Q_ERR_TIMEOUT: return "FP8Q_ERR_TIMEOUT";
+  }
+  return "FP8Q_ERR_UNKNOWN";
+}

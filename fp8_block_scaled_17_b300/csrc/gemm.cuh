@@ -1,0 +1,483 @@
+// Block-scaled FP8 GEMM with promotion of tensor-core partial sums every
+// 128 elements of K ("OMG! The most effective Deepseek Ever!", paragraph on
+// increased-precision accumulation: partial results are copied to FP32
+// registers on CUDA cores at a fixed interval, and the dequantization scales
+// are multiplied in there; "Don't Be Fooled By Deepseek Chatgpt", Figure 7 (b)).
+//
+// The pages describe two Hopper warpgroups whose WGMMA and promotion overlap.
+// On sm_103a the same overlap comes from tensor memory: the MMA of chunk kb+1
+// runs into one TMEM buffer while the promotion warps drain chunk kb from the
+// other.
+//
+// CTA tile 128 (M) x 256 (N); one 128-K chunk = 4 tcgen05.mma (K = 32 each).
+// Warp roles (384 threads = 3 warpgroups, one CTA per SM, persistent over tiles):
+//   warps 0-7  promotion + epilogue. Warp w reads TMEM lanes 32*(w%4).. (rows)
+//              and columns 128*(w/4).. of the tile: each thread owns one row and
+//              128 FP32 accumulators in registers. Per chunk it loads P_kb from
+//              TMEM and does acc += P_kb * (sa[kb][m] * sb[kb][n/128]).
+//   warp 8     TMA producer: A (128 x 128 B) and B (256 x 128 B) tiles into a
+//              4-stage shared-memory ring, 128-byte swizzled.
+//   warp 9     TMEM allocator + MMA issuer (one thread).
+//   warps 10-11 idle (they complete the third warpgroup).
+// Register split (setmaxnreg): the kernel is launched with 168 registers per
+// thread (384 x 168 = 64512); the producer/MMA warpgroup gives up to 40 and the
+// two promotion warpgroups rise to 232 (128 x 40 + 256 x 232 = 64512). The
+// host refuses to launch unless the compiled count is exactly kLaunchRegs.
+// Scales reach the promotion warps through a per-warp shared-memory ring fed
+// by cp.async three chunks ahead.
+//
+// Every wait is bounded in time. A wait that gives up raises a CTA-wide abort
+// flag and the device status word; all roles then stop, the producer waits for
+// its TMA loads in flight, the MMA issuer for its MMAs, and TMEM is freed
+// before the CTA exits.
+#pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace fp8q {
+
+// Error bits recorded by kernels (read and cleared by fp8q_get_status).
+constexpr unsigned kDevStatusTimeout = 1u;
+constexpr unsigned kDevStatusBadOffsets = 2u;
+
+namespace gemm {
+
+constexpr int BM = 128, BN = 256, BK = 128;
+constexpr int kStages = 4;
+constexpr int kABytes = BM * BK;  // 16 KB
+constexpr int kBBytes = BN * BK;  // 32 KB
+constexpr int kPromoWarps = 8;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kThreads = 384;
+constexpr int kLaunchRegs = 168;
+constexpr int kPromoRegs = 232;
+constexpr int kCtrlRegs = 40;
+static_assert(kThreads * kLaunchRegs >= 256 * kPromoRegs + 128 * kCtrlRegs,
+              "register split exceeds the launch budget");
+constexpr int kScaleSlots = 4;  // per promotion warp
+constexpr int kScaleAhead = 3;  // chunks of scales in flight
+constexpr int kSlotFloats = 32 + 128;
+constexpr uint32_t kTmemCols = 512;  // two 256-column accumulator buffers
+constexpr int kMaxExperts = 1024;
+
+constexpr int kFlagPromote = 1;
+constexpr int kFlagOutBF16 = 2;
+constexpr int kFlagScaleB1x128 = 4;
+
+struct Params {
+  const float* sa;            // [K/128][M]
+  const float* sb;            // [E][K/128][N/128] or, 1x128 mode, [K/128][N]
+  void* D;                    // [M][ldd]
+  const int32_t* m_offsets;   // [E+1] (device) or null for a dense GEMM
+  unsigned* status;           // device status word
+  int64_t M;                  // rows of A (Mtot)
+  int64_t ldd;
+  int N, K, E;
+  int flags;
+  int group_m;                // tile raster: M-tiles per group
+  uint32_t tx_bytes;          // bytes one stage's two TMA boxes deliver
+  uint64_t wait_limit_ns;
+  int inject_timeout;
+};
+
+struct Layout {
+  static constexpr uint32_t a_off = 0;
+  static constexpr uint32_t b_off = a_off + kStages * kABytes;
+  static constexpr uint32_t scale_off = b_off + kStages * kBBytes;
+  static constexpr uint32_t scale_bytes = kPromoWarps * kScaleSlots * kSlotFloats * 4;
+  static constexpr uint32_t bar_off = scale_off + scale_bytes;
+  static constexpr uint32_t n_bars = 2 * kStages + 6;
+  static constexpr uint32_t misc_off = bar_off + n_bars * 8;  // tmem base, abort flag
+  static constexpr uint32_t table_off = misc_off + 16;        // seg[E+1], prefix[E+1]
+  static constexpr uint32_t bytes(int E) { return table_off + 8u * (E + 1) + 1024u; }
+};
+
+struct Tile {
+  int64_t m0;     // first row of A (and D)
+  int64_t m_end;  // rows >= m_end belong to another expert / are padding
+  int n0;         // first column of D
+  int brow0;      // first row of B (expert-major)
+  int e;          // expert
+};
+
+// Tile t -> (expert, m-tile, n-tile). Within an expert, tiles are visited in
+// groups of group_m M-tiles, N fastest inside a group column, so that the CTAs
+// running at the same time share A rows and B columns in L2.
+__device__ __forceinline__ Tile tile_at(int t, const int* seg, const int* pre, int E, int nt,
+                                        int N, int group_m) {
+  int lo = 0, hi = E;  // pre[lo] <= t < pre[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (pre[mid] <= t) lo = mid; else hi = mid;
+  }
+  const int e = lo;
+  const int local = t - pre[e];
+  const int rows = seg[e + 1] - seg[e];
+  const int mt = (rows + BM - 1) / BM;
+  const int per_group = group_m * nt;
+  const int g = local / per_group;
+  const int first = g * group_m;
+  const int gs = min(mt - first, group_m);
+  const int r = local - g * per_group;
+  Tile tl;
+  tl.e = e;
+  tl.m0 = static_cast<int64_t>(seg[e]) + static_cast<int64_t>(first + r % gs) * BM;
+  tl.m_end = seg[e + 1];
+  tl.n0 = (r / gs) * BN;
+  tl.brow0 = e * N + tl.n0;
+  return tl;
+}
+
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
+                                             volatile uint32_t* abort_flag, const Params& p,
+                                             uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t n = 1;; ++n) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((n & 15u) == 0u) {
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 > limit_ns) {
+        *abort_flag = 1u;
+        atomicOr(p.status, kDevStatusTimeout);
+        return false;
+      }
+    }
+  }
+}
+
+// Used after an abort, to let work already in flight land (no abort check).
+__device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > limit_ns) return;
+  }
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// Position of the promotion warp's scale prefetch in its (tile, unit) stream.
+struct ScaleStream {
+  int t;       // tile
+  int u;       // unit (K-block, or 0 without promotion)
+  uint32_t n;  // units issued so far (ring slot = n % kScaleSlots)
+};
+
+// Copy (cp.async) the scales one promotion warp needs for the next unit of its
+// stream into its ring slot: sa of its 32 rows, and either the one 128x128
+// B-block scale of its column half or 128 per-column B scales. One commit
+// group per unit (empty past the last tile, so that group counting stays
+// uniform).
+__device__ __forceinline__ void issue_scales(ScaleStream& ss, const Params& p, const int* seg,
+                                             const int* pre, int nt, int KB, int NB, int units,
+                                             int total, bool promote, bool sb1, int q, int h,
+                                             int lane, uint32_t ring_s) {
+  const uint32_t dst = ring_s + (ss.n % kScaleSlots) * (kSlotFloats * 4);
+  if (ss.t < total) {
+    const Tile tl = tile_at(ss.t, seg, pre, p.E, nt, p.N, p.group_m);
+    const int kb = promote ? ss.u : 0;
+    const int64_t m = tl.m0 + q * 32 + lane;
+    const bool rok = m < tl.m_end;
+    cp_async_4(dst + 4u * lane, p.sa + static_cast<int64_t>(kb) * p.M + (rok ? m : 0),
+               rok ? 4u : 0u);
+    const int col0 = tl.n0 + h * 128;
+    const bool cok = col0 < p.N;
+    if (!sb1) {
+      if (lane == 0) {
+        const float* src =
+            p.sb + (static_cast<int64_t>(tl.e) * KB + kb) * NB + (cok ? col0 / 128 : 0);
+        cp_async_4(dst + 4u * 32, src, cok ? 4u : 0u);
+      }
+    } else {
+      const float* src = p.sb + static_cast<int64_t>(kb) * p.N + (cok ? col0 + 4 * lane : 0);
+      cp_async_16(dst + 4u * (32 + 4 * lane), src, cok ? 16u : 0u);
+    }
+  }
+  cp_async_commit();
+  ++ss.n;
+  if (++ss.u == units) {
+    ss.u = 0;
+    ss.t += gridDim.x;
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_blockscaled_kernel(const __grid_constant__ CUtensorMap tmA,
+                            const __grid_constant__ CUtensorMap tmB, const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* const base_ptr = smem_raw + (base - raw);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  const uint32_t bar0 = base + Layout::bar_off;
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (kStages + s); };
+  auto tfull_bar = [&](uint32_t b) { return bar0 + 8u * (2 * kStages + b); };
+  auto tempty_bar = [&](uint32_t b) { return bar0 + 8u * (2 * kStages + 2 + b); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * kStages + 4);
+  const uint32_t never_bar = bar0 + 8u * (2 * kStages + 5);
+  uint32_t* const misc = reinterpret_cast<uint32_t*>(base_ptr + Layout::misc_off);
+  volatile uint32_t* const abort_flag = misc + 1;
+  int* const seg = reinterpret_cast<int*>(base_ptr + Layout::table_off);
+  int* const pre = seg + (p.E + 1);
+
+  const int nt = (p.N + BN - 1) / BN;
+  const int KB = p.K / BK;
+  const bool promote = (p.flags & kFlagPromote) != 0;
+
+  // ---------------------------------------------------------------- setup
+  for (int e = threadIdx.x; e <= p.E; e += kThreads) {
+    seg[e] = p.m_offsets ? __ldg(p.m_offsets + e) : (e == 0 ? 0 : static_cast<int>(p.M));
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(base + Layout::misc_off, kTmemCols);
+    tmem_relinquish();
+  }
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (uint32_t b = 0; b < 2; ++b) {
+      mbar_init(tfull_bar(b), 1);
+      mbar_init(tempty_bar(b), kPromoWarps);
+    }
+    mbar_init(drain_bar, 1);
+    mbar_init(never_bar, 1);
+    misc[1] = 0u;
+    fence_mbar_init();
+  }
+  if (warp == kProducerWarp && lane == 0) {
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    // Clamp the segment offsets into [0, M], nondecreasing, and count tiles.
+    const int M = static_cast<int>(p.M);
+    bool bad = false;
+    int prev = 0;
+    for (int e = 0; e <= p.E; ++e) {
+      int v = seg[e];
+      if ((e == 0 && v != 0) || (e == p.E && v != M)) bad = true;
+      if (e == 0) v = 0;
+      if (e == p.E) v = M;
+      if (v < prev) { bad = true; v = prev; }
+      if (v > M) { bad = true; v = M; }
+      seg[e] = v;
+      prev = v;
+    }
+    pre[0] = 0;
+    for (int e = 0; e < p.E; ++e) pre[e + 1] = pre[e] + ((seg[e + 1] - seg[e] + BM - 1) / BM) * nt;
+    if (bad && blockIdx.x == 0) atomicOr(p.status, kDevStatusBadOffsets);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = misc[0];
+  const int total = pre[p.E];
+
+  if (warp >= kPromoWarps) {
+  setmaxnreg_dec<kCtrlRegs>();
+  if (warp == kProducerWarp) {
+    // ------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int issued = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        const Tile tl = tile_at(t, seg, pre, p.E, nt, p.N, p.group_m);
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, p, p.wait_limit_ns)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(full_bar(stage), p.tx_bytes);
+          tma_load_2d(base + Layout::a_off + stage * kABytes, &tmA, full_bar(stage), kb * BK,
+                      static_cast<int32_t>(tl.m0));
+          tma_load_2d(base + Layout::b_off + stage * kBBytes, &tmB, full_bar(stage), kb * BK,
+                      tl.brow0);
+          ++issued;
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        }
+      }
+      if (!ok) {  // let the loads still in flight land before the CTA exits
+        const int n = issued < kStages ? issued : kStages;
+        for (int i = 1; i <= n; ++i) {
+          int s = stage - i;
+          uint32_t ph = phase;
+          if (s < 0) { s += kStages; ph ^= 1u; }
+          wait_drain(full_bar(s), ph, p.wait_limit_ns);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    // ----------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_e4m3_f32(BM, BN);
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t unit = 0;
+      bool ok = true;
+      if (p.inject_timeout) ok = wait_bounded(never_bar, 0u, abort_flag, p, 20000000ull);
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        for (int kb = 0; kb < KB; ++kb) {
+          const uint32_t b = unit & 1u;
+          if (promote || kb == 0) {
+            if (!wait_bounded(tempty_bar(b), ((unit >> 1) & 1u) ^ 1u, abort_flag, p,
+                              p.wait_limit_ns)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+          }
+          if (!wait_bounded(full_bar(stage), phase, abort_flag, p, p.wait_limit_ns)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t adesc = sw128_kmajor_desc(base + Layout::a_off + stage * kABytes);
+          const uint64_t bdesc = sw128_kmajor_desc(base + Layout::b_off + stage * kBBytes);
+          const uint32_t d_tmem = tmem_base + b * BN;
+#pragma unroll
+          for (int k = 0; k < BK / 32; ++k) {
+            // advance 32 bytes of K inside the swizzled 128-byte rows
+            umma_f8f6f4(d_tmem, adesc + 2u * k, bdesc + 2u * k, idesc,
+                        (k > 0 || (!promote && kb > 0)) ? 1u : 0u);
+          }
+          umma_commit(empty_bar(stage));
+          if (promote || kb == KB - 1) {
+            umma_commit(tfull_bar(b));
+            ++unit;
+          }
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        }
+      }
+      if (!ok) {  // wait for the MMAs already issued
+        umma_commit(drain_bar);
+        wait_drain(drain_bar, 0u, p.wait_limit_ns);
+      }
+    }
+    __syncwarp();
+  }
+  } else {
+    setmaxnreg_inc<kPromoRegs>();
+    // ------------------------------------------------- promotion + epilogue
+    const int q = warp & 3;   // TMEM lane quarter -> rows 32q .. 32q+31
+    const int h = warp >> 2;  // column half -> columns 128h .. 128h+127
+    const bool sb1 = (p.flags & kFlagScaleB1x128) != 0;
+    const int NB = (p.N + 127) / 128;
+    const int units = promote ? KB : 1;
+    const float* const ring = reinterpret_cast<const float*>(base_ptr + Layout::scale_off) +
+                              warp * kScaleSlots * kSlotFloats;
+    const uint32_t ring_s = base + Layout::scale_off + warp * kScaleSlots * kSlotFloats * 4;
+
+    // scale prefetch stream over (tile, unit)
+    ScaleStream ss{static_cast<int>(blockIdx.x), 0, 0u};
+    for (int i = 0; i < kScaleAhead; ++i)
+      issue_scales(ss, p, seg, pre, nt, KB, NB, units, total, promote, sb1, q, h, lane, ring_s);
+
+    uint32_t unit = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      const Tile tl = tile_at(t, seg, pre, p.E, nt, p.N, p.group_m);
+      float acc[128];
+#pragma unroll
+      for (int j = 0; j < 128; ++j) acc[j] = 0.0f;
+
+      for (int u = 0; u < units; ++u) {
+        cp_async_wait<kScaleAhead - 1>();
+        __syncwarp();
+        const float* slot = ring + (unit % kScaleSlots) * kSlotFloats;
+        const float sa_v = slot[lane];
+        const uint32_t b = unit & 1u;
+        // every lane waits; the vote keeps the warp-collective TMEM loads uniform
+        const bool got = wait_bounded(tfull_bar(b), (unit >> 1) & 1u, abort_flag, p,
+                                      p.wait_limit_ns);
+        if (!__all_sync(0xffffffffu, got)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + b * BN + h * 128;
+        const float s_blk = sb1 ? 0.0f : __fmul_rn(sa_v, slot[32]);
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint32_t r0[32], r1[32];
+          tmem_ld_32x32b_x32(taddr + half * 64, r0);
+          tmem_ld_32x32b_x32(taddr + half * 64 + 32, r1);
+          tmem_ld_wait();
+          if (half == 1) {  // buffer fully read: hand it back to the MMA issuer
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty_bar(b));
+          }
+          if (!sb1) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              acc[half * 64 + j] = fmaf(__uint_as_float(r0[j]), s_blk, acc[half * 64 + j]);
+              acc[half * 64 + 32 + j] =
+                  fmaf(__uint_as_float(r1[j]), s_blk, acc[half * 64 + 32 + j]);
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const float s0 = __fmul_rn(sa_v, slot[32 + half * 64 + j]);
+              const float s1 = __fmul_rn(sa_v, slot[32 + half * 64 + 32 + j]);
+              acc[half * 64 + j] = fmaf(__uint_as_float(r0[j]), s0, acc[half * 64 + j]);
+              acc[half * 64 + 32 + j] =
+                  fmaf(__uint_as_float(r1[j]), s1, acc[half * 64 + 32 + j]);
+            }
+          }
+        }
+        ++unit;
+        issue_scales(ss, p, seg, pre, nt, KB, NB, units, total, promote, sb1, q, h, lane, ring_s);
+      }
+      if (!ok) break;
+
+      // ---------------------------------------------------------- epilogue
+      const int64_t m = tl.m0 + q * 32 + lane;
+      const int col0 = tl.n0 + h * 128;
+      if (m < tl.m_end && col0 < p.N) {
+        if (p.flags & kFlagOutBF16) {
+          uint4* d = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.D) + m * p.ldd + col0);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            d[j] = make_uint4(pack_bf16x2(acc[8 * j + 0], acc[8 * j + 1]),
+                              pack_bf16x2(acc[8 * j + 2], acc[8 * j + 3]),
+                              pack_bf16x2(acc[8 * j + 4], acc[8 * j + 5]),
+                              pack_bf16x2(acc[8 * j + 6], acc[8 * j + 7]));
+          }
+        } else {
+          float4* d = reinterpret_cast<float4*>(static_cast<float*>(p.D) + m * p.ldd + col0);
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            d[j] = make_float4(acc[4 * j], acc[4 * j + 1], acc[4 * j + 2], acc[4 * j + 3]);
+        }
+      }
+    }
+    cp_async_wait<0>();
+  }
+
+  // ---------------------------------------------------------------- teardown
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+}  // namespace gemm
+}  // namespace fp8q

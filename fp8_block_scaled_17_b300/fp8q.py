@@ -1,0 +1,171 @@
+"""Python binding of libfp8q.so (C ABI in include/fp8q.h).
+
+Argument marshalling only: every computation runs in the library's CUDA
+kernels. PyTorch provides device memory and the current CUDA stream. Output
+tensors are allocated here with torch unless the caller passes them in.
+
+Importing this module loads the library and raises if it has not been built:
+there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libfp8q.so")
+
+# status codes and flags (fp8q.h)
+OK, ERR_INVALID_ARG, ERR_SHAPE, ERR_ALIGN, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT = range(7)
+POW2_SCALE = 1
+TRANSPOSED_INPUT = 2
+SCALE_B_1x128 = 4
+NO_PROMOTION = 8
+OUT_BF16 = 16
+
+EXPORTED = ("fp8q_quant_act_1x128", "fp8q_quant_w_128x128", "fp8q_requant_1x128_to_128x1",
+            "fp8q_gemm_blockscaled", "fp8q_grouped_gemm", "fp8q_get_status",
+            "fp8q_status_string")
+
+
+class Fp8qError(RuntimeError):
+    def __init__(self, status: int, call: str):
+        self.status = status
+        super().__init__(f"{call}: {status_string(status)}")
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(_LIB_PATH):
+        raise ImportError(f"{_LIB_PATH} is not built; run `python -m "
+                          "fp8_block_scaled_17_b300.build` (nvcc, sm_103a)")
+    lib = ctypes.CDLL(_LIB_PATH)
+    vp, i64, u32, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_uint, ctypes.c_int
+    sig = {
+        "fp8q_quant_act_1x128": [vp, i64, i64, i64, vp, i64, vp, u32, vp],
+        "fp8q_quant_w_128x128": [vp, i64, i64, vp, vp, u32, vp],
+        "fp8q_requant_1x128_to_128x1": [vp, vp, i64, i64, vp, vp, u32, vp],
+        "fp8q_gemm_blockscaled": [vp, vp, vp, vp, i64, i64, i64, vp, i64, u32, vp],
+        "fp8q_grouped_gemm": [vp, vp, vp, i32, vp, vp, i64, i64, i64, vp, u32, vp],
+        "fp8q_get_status": [vp],
+        "fp8q_status_string": [i32],
+    }
+    for name, args in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = ctypes.c_char_p if name == "fp8q_status_string" else ctypes.c_int
+    return lib
+
+
+LIB = _load()
+
+
+def status_string(status: int) -> str:
+    return LIB.fp8q_status_string(int(status)).decode()
+
+
+def _stream(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t: torch.Tensor | None):
+    return ctypes.c_void_p(0 if t is None else t.data_ptr())
+
+
+def _check(status: int, call: str):
+    if status != OK:
+        raise Fp8qError(status, call)
+
+
+def get_status(stream=None) -> int:
+    """Synchronizes the stream and returns (and clears) device-side errors."""
+    return LIB.fp8q_get_status(_stream(stream))
+
+
+# ---------------------------------------------------------------- quantizers
+def quant_act_1x128(x: torch.Tensor, pow2: bool = False, transposed_input: bool = False,
+                    q: torch.Tensor | None = None, sa: torch.Tensor | None = None, stream=None):
+    """x bf16 [M][K] (or [K][M] with transposed_input) -> (codes u8 [M][K],
+    scales f32 [K/128][M])."""
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
+    if transposed_input:
+        K, M = x.shape
+    else:
+        M, K = x.shape
+    if q is None:
+        q = torch.empty((M, K), dtype=torch.uint8, device=x.device)
+    if sa is None:
+        sa = torch.empty((K // 128, M), dtype=torch.float32, device=x.device)
+    flags = (POW2_SCALE if pow2 else 0) | (TRANSPOSED_INPUT if transposed_input else 0)
+    _check(LIB.fp8q_quant_act_1x128(_ptr(x), M, K, x.stride(0), _ptr(q), q.stride(0), _ptr(sa),
+                                    flags, _stream(stream)), "fp8q_quant_act_1x128")
+    return q, sa
+
+
+def quant_w_128x128(w: torch.Tensor, pow2: bool = False, q: torch.Tensor | None = None,
+                    sb: torch.Tensor | None = None, stream=None):
+    """w bf16 [K][N] -> (codes u8 [N][K], scales f32 [K/128][N/128])."""
+    assert w.dtype == torch.bfloat16 and w.dim() == 2 and w.is_contiguous()
+    K, N = w.shape
+    if q is None:
+        q = torch.empty((N, K), dtype=torch.uint8, device=w.device)
+    if sb is None:
+        sb = torch.empty((K // 128, N // 128), dtype=torch.float32, device=w.device)
+    _check(LIB.fp8q_quant_w_128x128(_ptr(w), K, N, _ptr(q), _ptr(sb),
+                                    POW2_SCALE if pow2 else 0, _stream(stream)),
+           "fp8q_quant_w_128x128")
+    return q, sb
+
+
+def requant_1x128_to_128x1(q_in: torch.Tensor, s_in: torch.Tensor, pow2: bool = False,
+                           q_out: torch.Tensor | None = None, s_out: torch.Tensor | None = None,
+                           stream=None):
+    """codes [T][C] + scales [C/128][T] -> (codes [C][T], scales [T/128][C])."""
+    assert q_in.dtype == torch.uint8 and q_in.is_contiguous() and s_in.is_contiguous()
+    T, C = q_in.shape
+    if q_out is None:
+        q_out = torch.empty((C, T), dtype=torch.uint8, device=q_in.device)
+    if s_out is None:
+        s_out = torch.empty((T // 128, C), dtype=torch.float32, device=q_in.device)
+    _check(LIB.fp8q_requant_1x128_to_128x1(_ptr(q_in), _ptr(s_in), T, C, _ptr(q_out),
+                                           _ptr(s_out), POW2_SCALE if pow2 else 0,
+                                           _stream(stream)), "fp8q_requant_1x128_to_128x1")
+    return q_out, s_out
+
+
+# --------------------------------------------------------------------- GEMMs
+def gemm_blockscaled(a: torch.Tensor, sa: torch.Tensor, b: torch.Tensor, sb: torch.Tensor,
+                     out_dtype=torch.bfloat16, scale_b_1x128: bool = False,
+                     no_promotion: bool = False, d: torch.Tensor | None = None, stream=None):
+    """codes a [M][K], b [N][K] with scales -> D [M][N] (bf16 or f32)."""
+    assert a.dtype == torch.uint8 and b.dtype == torch.uint8
+    assert a.is_contiguous() and b.is_contiguous() and sa.is_contiguous() and sb.is_contiguous()
+    M, K = a.shape
+    N = b.shape[0]
+    if d is None:
+        d = torch.empty((M, N), dtype=out_dtype, device=a.device)
+    flags = ((OUT_BF16 if d.dtype == torch.bfloat16 else 0) |
+             (SCALE_B_1x128 if scale_b_1x128 else 0) | (NO_PROMOTION if no_promotion else 0))
+    _check(LIB.fp8q_gemm_blockscaled(_ptr(a), _ptr(sa), _ptr(b), _ptr(sb), M, N, K, _ptr(d),
+                                     d.stride(0), flags, _stream(stream)),
+           "fp8q_gemm_blockscaled")
+    return d
+
+
+def grouped_gemm(a: torch.Tensor, sa: torch.Tensor, m_offsets: torch.Tensor, b: torch.Tensor,
+                 sb: torch.Tensor, out_dtype=torch.bfloat16, no_promotion: bool = False,
+                 d: torch.Tensor | None = None, stream=None):
+    """expert-sorted codes a [Mtot][K], m_offsets int32 [E+1] (device),
+    b [E][N][K], sb [E][K/128][N/128] -> D [Mtot][N]."""
+    assert m_offsets.dtype == torch.int32 and m_offsets.is_cuda
+    assert a.is_contiguous() and b.is_contiguous() and sa.is_contiguous() and sb.is_contiguous()
+    Mtot, K = a.shape
+    E, N, _ = b.shape
+    if d is None:
+        d = torch.empty((Mtot, N), dtype=out_dtype, device=a.device)
+    assert d.is_contiguous()
+    flags = (OUT_BF16 if d.dtype == torch.bfloat16 else 0) | (NO_PROMOTION if no_promotion else 0)
+    _check(LIB.fp8q_grouped_gemm(_ptr(a), _ptr(sa), _ptr(m_offsets), E, _ptr(b), _ptr(sb), Mtot,
+                                 N, K, _ptr(d), flags, _stream(stream)), "fp8q_grouped_gemm")
+    return d

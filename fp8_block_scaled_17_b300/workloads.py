@@ -87,6 +87,18 @@ def ksweep_problem(K: int) -> GemmProblem:
     return GemmProblem(f"k-sweep 4096x4096x{K}", 4096, 4096, K, 1.0, 1.0, 0.0, 1.0, "f32")
 
 
+def ksweep_operand(rows: int, K: int, seed: int) -> torch.Tensor:
+    """bf16 [rows][K] ~ N(0, 1) clipped to +-6, with the first entry of every
+    128-element row tile set to 6. Every 1x128 tile then has max-abs exactly 6,
+    so power-of-two tile scales are all 2^-6: one scale for the whole tensor,
+    which is what the accumulation study needs (the promoted and the
+    tensor-core-only GEMM then see identical codes and constant scales)."""
+    g = torch.Generator().manual_seed(seed)
+    x = torch.randn((rows, K), generator=g, dtype=torch.float32).clamp_(-6.0, 6.0)
+    x[:, ::128] = 6.0
+    return x.to(torch.bfloat16)
+
+
 @dataclass
 class MoeProblem:
     """MoE up-projection: E experts with W_e [K][N]; tokens x topk routed rows."""

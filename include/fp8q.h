@@ -1,0 +1,175 @@
+/*
+ * fp8q.h -- C ABI of libfp8q.so: fine-grained (block-scaled) FP8 E4M3
+ * quantization and a block-scaled FP8 GEMM that promotes tensor-core partial
+ * sums into FP32 every 128 elements of K, for NVIDIA B300 (sm_103a).
+ *
+ * Sources, cited by page title (or host name where the page prints no title):
+ *   [WHY-BE]  why-be.co.kr board post 61844: online max-abs per 1x128
+ *             activation tile / 128x128 weight block; E4M3 on all tensors;
+ *             FP8 activation caching; 1x128 -> 128x1 re-tiling in the backward
+ *             pass; integral power-of-2 scaling factors.
+ *   [OMG]     "OMG! The most effective Deepseek Ever!": scaling the max-abs to
+ *             the FP8 maximum; promotion of tensor-core partial sums to FP32
+ *             registers at a fixed interval with dequantization folded in;
+ *             Figure 6 (Fprop, Dgrad, Wgrad in FP8).
+ *   [FOOLED]  "Don't Be Fooled By Deepseek Chatgpt": promotion to CUDA cores,
+ *             Figure 7 (b).
+ *   [HEARAON] hearaon.co.kr board post 810961: activations quantized to FP8
+ *             before MoE dispatch and up-projection; Hopper's 14-bit
+ *             fixed-point FP8 accumulation.
+ *
+ * Conventions shared by every call
+ *   - Codes are uint8 E4M3 ("fn": bias 7, no infinity, 0x7F/0xFF NaN, max
+ *     448), round-to-nearest-even with saturation to +-448. Scales are float32
+ *     DEQUANTIZATION scales: value ~= dec(code) * scale. A tile's scale is
+ *     s = max(RN32(amax / 448), 2^-126), or with FP8Q_POW2_SCALE the least
+ *     power of two 2^p (p >= -126) with amax <= 448 * 2^p; codes are
+ *     enc(RN32(x / s)) with IEEE float32 division. Inputs must be finite.
+ *   - All pointers are DEVICE pointers owned by the caller. The library
+ *     allocates no device memory; it keeps only host-side state (function
+ *     attributes, the tensor-map encoder entry point) and one device status
+ *     word per device.
+ *   - Every call is asynchronous on `stream` (NULL = legacy default stream).
+ *     Argument, shape, alignment and flag errors are returned synchronously
+ *     before anything is launched; a failed launch returns FP8Q_ERR_CUDA.
+ *     Errors detected on the device (a pipeline wait that exceeded its time
+ *     limit, malformed grouped-GEMM offsets) are reported by fp8q_get_status.
+ *   - "16-byte aligned" applies to the base pointer and to every row
+ *     (leading dimension x element size a multiple of 16).
+ */
+#ifndef FP8Q_H
+#define FP8Q_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; declared here so that the header needs no CUDA
+ * headers. */
+typedef struct CUstream_st* fp8q_stream_t;
+
+typedef enum {
+  FP8Q_OK = 0,
+  FP8Q_ERR_INVALID_ARG = 1, /* null pointer, unknown flag, bad offsets       */
+  FP8Q_ERR_SHAPE = 2,       /* a dimension or leading dimension is invalid  */
+  FP8Q_ERR_ALIGN = 3,       /* a pointer or row is not 16-byte aligned      */
+  FP8Q_ERR_UNSUPPORTED = 4, /* device is not sm_103 / sm_100 class          */
+  FP8Q_ERR_CUDA = 5,        /* a CUDA runtime or driver call failed         */
+  FP8Q_ERR_TIMEOUT = 6      /* a device-side pipeline wait hit its limit    */
+} fp8q_status;
+
+enum {
+  FP8Q_POW2_SCALE = 1,       /* quantizers: power-of-two scales [WHY-BE]     */
+  FP8Q_TRANSPOSED_INPUT = 2, /* quant_act: x is stored [K][M]                */
+  FP8Q_SCALE_B_1x128 = 4,    /* GEMM: B has one scale per (column, K-block)  */
+  FP8Q_NO_PROMOTION = 8,     /* GEMM: accumulate all of K in the tensor core */
+  FP8Q_OUT_BF16 = 16         /* GEMM: bf16 output (default float32)          */
+};
+
+/*
+ * 1x128 activation quantization [WHY-BE; OMG, paragraph on grouping].
+ * x    : bf16 [M][K] with row stride ldx elements (ldx >= K); with
+ *        FP8Q_TRANSPOSED_INPUT, x is stored [K][M] with row stride ldx >= M
+ *        and the tiles run down K (128x1 tiles of the stored array: the
+ *        output-gradient layout that Wgrad contracts over tokens).
+ * q    : uint8 codes [M][K], row stride ldq bytes (ldq >= K).
+ * sa   : float32 [K/128][M]: scale of row m, K-block kb at sa[kb*M + m].
+ * M >= 0 (any value; M == 0 is a no-op), K > 0 and K % 128 == 0.
+ * x and q 16-byte aligned (rows included); sa 4-byte aligned.
+ * flags: FP8Q_POW2_SCALE | FP8Q_TRANSPOSED_INPUT.
+ */
+fp8q_status fp8q_quant_act_1x128(const void* x, int64_t M, int64_t K, int64_t ldx,
+                                 uint8_t* q, int64_t ldq, float* sa, unsigned flags,
+                                 fp8q_stream_t stream);
+
+/*
+ * 128x128 weight-block quantization [WHY-BE].
+ * w  : bf16 [K][N] row-major (input channels x output channels), contiguous.
+ * q  : uint8 codes [N][K] (transposed: K-major, the GEMM's B operand).
+ * sb : float32 [K/128][N/128], one scale per 128x128 block.
+ * K % 128 == 0 and N % 128 == 0, both > 0. w, q 16-byte aligned.
+ * flags: FP8Q_POW2_SCALE.
+ */
+fp8q_status fp8q_quant_w_128x128(const void* w, int64_t K, int64_t N, uint8_t* q,
+                                 float* sb, unsigned flags, fp8q_stream_t stream);
+
+/*
+ * Backward-pass re-tiling of a cached FP8 activation from 1x128 to 128x1
+ * tiles [WHY-BE, paragraph "transformed from an 1x128 quantization tile to an
+ * 128x1 tile in the backward pass"; paragraph on caching activations in FP8].
+ * q_in  : uint8 codes [T][C] (1x128 tiles along C), s_in float32 [C/128][T].
+ * Each value is dequantized as x' = RN32(dec(q) * s_row) and re-quantized
+ * with one scale per 128 tokens of one channel.
+ * q_out : uint8 codes [C][T] (transposed: T-major, so Wgrad contracts over
+ *         contiguous tokens); s_out float32 [T/128][C].
+ * T % 128 == 0 and C % 128 == 0, both > 0; q_in, q_out 16-byte aligned.
+ * flags: FP8Q_POW2_SCALE (apply the power-of-two rule to the new tiles).
+ */
+fp8q_status fp8q_requant_1x128_to_128x1(const uint8_t* q_in, const float* s_in, int64_t T,
+                                        int64_t C, uint8_t* q_out, float* s_out,
+                                        unsigned flags, fp8q_stream_t stream);
+
+/*
+ * Block-scaled FP8 GEMM with promotion every 128 K [OMG, paragraph on
+ * increased-precision accumulation; FOOLED, Figure 7 (b)]:
+ *   D[m][n] = sum_kb P_kb[m][n] * (sa[kb][m] * sbv[kb][n]),
+ *   P_kb = sum over the 128 k of block kb of dec(A[m][k]) * dec(B[n][k]),
+ * P_kb is formed on the tensor cores (tcgen05, FP32 in tensor memory) and
+ * every P_kb is scaled and added to an FP32 register accumulator.
+ * A  : uint8 codes [M][K] (K-major), sa float32 [K/128][M].
+ * B  : uint8 codes [N][K] (K-major);
+ *      default: sb float32 [K/128][N/128] (128x128 blocks, sbv = sb[kb][n/128]);
+ *      FP8Q_SCALE_B_1x128: sb float32 [K/128][N] (sbv = sb[kb][n]), the Wgrad
+ *      case where both operands are 1x128 along K. sb 16-byte aligned then.
+ * D  : [M][ldd], float32, or bf16 with FP8Q_OUT_BF16 (round to nearest even).
+ * FP8Q_NO_PROMOTION: the whole K is accumulated in the tensor core and the
+ *      scales of K-block 0 are applied once at the end; correct only when the
+ *      scales are constant along K (the accumulation study's variant).
+ * M >= 0 (any value), N > 0 with N % 128 == 0, K > 0 with K % 128 == 0,
+ * ldd >= N. A, B, D 16-byte aligned; sa, sb 4-byte aligned.
+ */
+fp8q_status fp8q_gemm_blockscaled(const uint8_t* A, const float* sa, const uint8_t* B,
+                                  const float* sb, int64_t M, int64_t N, int64_t K, void* D,
+                                  int64_t ldd, unsigned flags, fp8q_stream_t stream);
+
+/*
+ * Grouped GEMM for MoE experts [HEARAON, paragraph on FP8 quantization before
+ * MoE up-projection and dispatch; OMG, same paragraph]: rows
+ * m_offsets[e] .. m_offsets[e+1]-1 of A (expert-sorted tokens) are multiplied
+ * by expert e's weight B[e]. Same arithmetic as fp8q_gemm_blockscaled.
+ * A         : uint8 codes [Mtot][K], sa float32 [K/128][Mtot].
+ * m_offsets : DEVICE int32 [E+1], nondecreasing, m_offsets[0] = 0,
+ *             m_offsets[E] = Mtot; empty experts allowed. Read on the device
+ *             only (no host synchronisation); violations are clamped and
+ *             reported by fp8q_get_status as FP8Q_ERR_INVALID_ARG.
+ * B         : uint8 codes [E][N][K]; sb float32 [E][K/128][N/128].
+ * D         : [Mtot][N] contiguous, float32 or bf16 (FP8Q_OUT_BF16).
+ * 1 <= E <= 1024. Flags: FP8Q_OUT_BF16 | FP8Q_NO_PROMOTION.
+ */
+fp8q_status fp8q_grouped_gemm(const uint8_t* A, const float* sa, const int32_t* m_offsets,
+                              int E, const uint8_t* B, const float* sb, int64_t Mtot, int64_t N,
+                              int64_t K, void* D, unsigned flags, fp8q_stream_t stream);
+
+/*
+ * Synchronizes `stream`, then reports (and clears) errors that kernels of the
+ * current device recorded: FP8Q_ERR_TIMEOUT if a pipeline wait exceeded its
+ * limit (the kernel stopped early: its outputs are invalid, the context stays
+ * usable), FP8Q_ERR_INVALID_ARG for malformed grouped-GEMM offsets,
+ * FP8Q_ERR_CUDA if the stream reported a CUDA error. No counterpart in the
+ * pages: this is the library's failure-detection hook.
+ * Debugging aid: with the environment variable FP8Q_DEBUG_INJECT_TIMEOUT=1 set
+ * when a GEMM is called, that GEMM waits on a barrier that nothing signals,
+ * gives up after 20 ms and takes the timeout path.
+ */
+fp8q_status fp8q_get_status(fp8q_stream_t stream);
+
+/* Human-readable name of a status code (static storage). */
+const char* fp8q_status_string(fp8q_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8Q_H */

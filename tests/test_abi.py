@@ -1,0 +1,97 @@
+"""The C ABI: libfp8q.so loads without a GPU, exports exactly the entry points
+include/fp8q.h declares, and rejects bad arguments on the host before any
+CUDA call (these checks need no GPU)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fp8q.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from fp8_block_scaled_17_b300 import build
+    build.build()
+    from fp8_block_scaled_17_b300 import fp8q
+    return fp8q
+
+
+def header_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fp8q_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    funcs = header_functions()
+    for name in ("fp8q_quant_act_1x128", "fp8q_quant_w_128x128", "fp8q_requant_1x128_to_128x1",
+                 "fp8q_gemm_blockscaled", "fp8q_grouped_gemm", "fp8q_get_status",
+                 "fp8q_status_string"):
+        assert name in funcs
+
+
+def test_library_exports_exactly_the_header(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", lib._LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = sorted({l.split()[-1] for l in out.splitlines()
+                       if l.split()[-1].startswith("fp8q_")})
+    assert exported == header_functions()
+    for name in exported:
+        assert hasattr(lib.LIB, name)
+
+
+def test_status_strings(lib):
+    for code in range(7):
+        assert lib.status_string(code).startswith("FP8Q_")
+
+
+NULL = ctypes.c_void_p(0)
+FAKE = ctypes.c_void_p(1 << 20)       # never dereferenced: validation fails first
+MISALIGNED = ctypes.c_void_p((1 << 20) + 4)
+
+
+def test_quant_act_host_validation(lib):
+    L = lib.LIB
+    assert L.fp8q_quant_act_1x128(FAKE, 8, 100, 128, FAKE, 128, FAKE, 0, NULL) == lib.ERR_SHAPE
+    assert L.fp8q_quant_act_1x128(FAKE, 8, 128, 64, FAKE, 128, FAKE, 0, NULL) == lib.ERR_SHAPE
+    assert L.fp8q_quant_act_1x128(FAKE, 8, 128, 128, FAKE, 128, FAKE, 64, NULL) == lib.ERR_INVALID_ARG
+    assert L.fp8q_quant_act_1x128(NULL, 8, 128, 128, FAKE, 128, FAKE, 0, NULL) == lib.ERR_INVALID_ARG
+    assert L.fp8q_quant_act_1x128(MISALIGNED, 8, 128, 128, FAKE, 128, FAKE, 0, NULL) == lib.ERR_ALIGN
+    assert L.fp8q_quant_act_1x128(FAKE, 8, 128, 132, FAKE, 128, FAKE, 0, NULL) == lib.ERR_ALIGN
+    assert L.fp8q_quant_act_1x128(FAKE, -1, 128, 128, FAKE, 128, FAKE, 0, NULL) == lib.ERR_SHAPE
+    # M == 0 is a no-op that touches nothing
+    assert L.fp8q_quant_act_1x128(NULL, 0, 128, 128, NULL, 128, NULL, 0, NULL) == lib.OK
+    # transposed input: ldx must cover M
+    assert L.fp8q_quant_act_1x128(FAKE, 300, 128, 256, FAKE, 128, FAKE, 2, NULL) == lib.ERR_SHAPE
+
+
+def test_quant_w_and_requant_host_validation(lib):
+    L = lib.LIB
+    assert L.fp8q_quant_w_128x128(FAKE, 128, 100, FAKE, FAKE, 0, NULL) == lib.ERR_SHAPE
+    assert L.fp8q_quant_w_128x128(FAKE, 128, 128, FAKE, FAKE, 2, NULL) == lib.ERR_INVALID_ARG
+    assert L.fp8q_quant_w_128x128(FAKE, 128, 128, MISALIGNED, FAKE, 0, NULL) == lib.ERR_ALIGN
+    assert L.fp8q_requant_1x128_to_128x1(FAKE, FAKE, 100, 128, FAKE, FAKE, 0, NULL) == lib.ERR_SHAPE
+    assert L.fp8q_requant_1x128_to_128x1(FAKE, NULL, 128, 128, FAKE, FAKE, 0, NULL) == lib.ERR_INVALID_ARG
+
+
+def test_gemm_host_validation(lib):
+    L = lib.LIB
+    g = L.fp8q_gemm_blockscaled
+    assert g(FAKE, FAKE, FAKE, FAKE, 16, 100, 128, FAKE, 100, 0, NULL) == lib.ERR_SHAPE  # N % 128
+    assert g(FAKE, FAKE, FAKE, FAKE, 16, 128, 96, FAKE, 128, 0, NULL) == lib.ERR_SHAPE   # K % 128
+    assert g(FAKE, FAKE, FAKE, FAKE, 16, 128, 128, FAKE, 64, 0, NULL) == lib.ERR_SHAPE   # ldd < N
+    assert g(FAKE, FAKE, FAKE, FAKE, 16, 128, 128, FAKE, 128, 1, NULL) == lib.ERR_INVALID_ARG
+    assert g(FAKE, FAKE, MISALIGNED, FAKE, 16, 128, 128, FAKE, 128, 0, NULL) == lib.ERR_ALIGN
+    assert g(FAKE, FAKE, FAKE, FAKE, 16, 128, 128, FAKE, 132, 16, NULL) == lib.ERR_ALIGN  # bf16 row
+    assert g(NULL, FAKE, FAKE, FAKE, 16, 128, 128, FAKE, 128, 0, NULL) == lib.ERR_INVALID_ARG
+    assert g(NULL, NULL, NULL, NULL, 0, 128, 128, NULL, 128, 0, NULL) == lib.OK  # M == 0
+    gg = L.fp8q_grouped_gemm
+    assert gg(FAKE, FAKE, NULL, 4, FAKE, FAKE, 64, 128, 128, FAKE, 0, NULL) == lib.ERR_INVALID_ARG
+    assert gg(FAKE, FAKE, FAKE, 0, FAKE, FAKE, 64, 128, 128, FAKE, 0, NULL) == lib.ERR_SHAPE
+    assert gg(FAKE, FAKE, FAKE, 2000, FAKE, FAKE, 64, 128, 128, FAKE, 0, NULL) == lib.ERR_SHAPE
+    # the 1x128 B-scale mode belongs to the dense GEMM only
+    assert gg(FAKE, FAKE, FAKE, 4, FAKE, FAKE, 64, 128, 128, FAKE, 4, NULL) == lib.ERR_INVALID_ARG

@@ -1,0 +1,171 @@
+"""GPU block-scaled GEMM vs the CPU oracle, within
+max|gpu - oracle| <= 1e-4 * ||a_i|| * ||b_j|| + 1 ulp of the output format."""
+import numpy as np
+import pytest
+import torch
+
+import oracle.fp8q_oracle as O
+from fp8_block_scaled_17_b300 import workloads as W
+from tests.helpers import assert_gemm_close, check_gemm_sampled, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def F(cuda_device):
+    from fp8_block_scaled_17_b300 import fp8q
+    return fp8q
+
+
+def _quantized_problem(F, M, N, K, seed, a_std=1.0, w_std=0.02, outlier_frac=0.001,
+                       outlier_scale=100.0):
+    a = W.bf16_normal((M, K), a_std, seed, outlier_frac, outlier_scale).cuda()
+    w = W.bf16_normal((K, N), w_std, seed + 1).cuda()
+    qa, sa = F.quant_act_1x128(a)
+    qb, sb = F.quant_w_128x128(w)
+    return qa, sa, qb, sb
+
+
+def _full_check(d, qa, sa, qb, sb, out, scale_b="128x128"):
+    qa, sa, qb, sb = (x.cpu().numpy() for x in (qa, sa, qb, sb))
+    ref = O.gemm_blockscaled(qa, sa, qb, sb, scale_b)
+    na, nb = O.row_col_norms(qa, sa, qb, sb, scale_b)
+    return assert_gemm_close(to_np(d), ref, na, nb, out)
+
+
+def test_tiny_config(F):
+    """A [256][512] N(0,1) with 0.1% x100 outliers, B [512][256] N(0, 0.02^2),
+    1x128 / 128x128 scales, FP32 output."""
+    p = W.TINY
+    a, w = p.make()
+    qa, sa = F.quant_act_1x128(a.cuda())
+    qb, sb = F.quant_w_128x128(w.cuda())
+    d = F.gemm_blockscaled(qa, sa, qb, sb, out_dtype=torch.float32)
+    _full_check(d, qa, sa, qb, sb, "f32")
+
+
+@pytest.mark.parametrize("M,N,K,out", [(300, 384, 640, "bf16"), (1, 128, 128, "f32"),
+                                       (129, 256, 256, "f32"), (700, 1024, 1152, "bf16"),
+                                       (37, 640, 384, "bf16")])
+def test_ragged_shapes(F, M, N, K, out):
+    qa, sa, qb, sb = _quantized_problem(F, M, N, K, seed=M + N + K)
+    dt = torch.bfloat16 if out == "bf16" else torch.float32
+    d = F.gemm_blockscaled(qa, sa, qb, sb, out_dtype=dt)
+    _full_check(d, qa, sa, qb, sb, out)
+
+
+def test_strided_output(F):
+    qa, sa, qb, sb = _quantized_problem(F, 200, 256, 512, seed=5)
+    big = torch.full((200, 384), 7.0, dtype=torch.float32, device="cuda")
+    F.gemm_blockscaled(qa, sa, qb, sb, d=big[:, 64:320])
+    _full_check(big[:, 64:320], qa, sa, qb, sb, "f32")
+    assert (big[:, :64] == 7).all() and (big[:, 320:] == 7).all()
+
+
+def test_exact_integer_inputs(F):
+    """Integer entries |v| <= 16 with one +-448 per tile: every scale is 1 and
+    every partial sum is an integer below 2^24, so the result must equal int64
+    matmul exactly (this also probes the tensor core's accumulation inside a
+    128-K chunk)."""
+    g = np.random.default_rng(1)
+    M, N, K = 256, 512, 1024
+    A = g.integers(-16, 17, (M, K)).astype(np.float32)
+    Wt = g.integers(-16, 17, (K, N)).astype(np.float32)
+    for kb in range(K // 128):
+        A[:, kb * 128 + g.integers(0, 128)] = 448.0
+        for nb in range(N // 128):
+            Wt[kb * 128 + 3, nb * 128 + 11] = -448.0
+    qa, sa = F.quant_act_1x128(torch.from_numpy(A).to(torch.bfloat16).cuda())
+    qb, sb = F.quant_w_128x128(torch.from_numpy(Wt).to(torch.bfloat16).cuda())
+    assert (sa == 1).all() and (sb == 1).all()
+    d = F.gemm_blockscaled(qa, sa, qb, sb, out_dtype=torch.float32)
+    want = A.astype(np.int64) @ Wt.astype(np.int64)
+    assert np.abs(want).max() < 2 ** 24
+    assert (to_np(d).astype(np.int64) == want).all()
+
+
+def test_scale_b_1x128(F):
+    """Wgrad form: both operands 1x128 along K (per-column B scales)."""
+    M, N, K = 300, 384, 1024
+    x = W.bf16_normal((K, M), 1.0, seed=11).cuda()    # [tokens][channels]
+    dy = W.bf16_normal((K, N), 1e-3, seed=12).cuda()
+    qa, sa = F.quant_act_1x128(x, True, transposed_input=True)
+    qb, sb = F.quant_act_1x128(dy, False, transposed_input=True)
+    d = F.gemm_blockscaled(qa, sa, qb, sb, out_dtype=torch.float32, scale_b_1x128=True)
+    _full_check(d, qa, sa, qb, sb, "f32", "1x128")
+
+
+def test_wgrad_path_small(F):
+    """Requant (1x128 -> 128x1) of a cached activation feeding the Wgrad GEMM."""
+    T, C, Co = 512, 256, 384
+    x = W.bf16_normal((T, C), 1.0, seed=21).cuda()
+    dy = W.bf16_normal((T, Co), 1e-3, seed=22).cuda()
+    qx, sx = F.quant_act_1x128(x, True)
+    qa, sa = F.requant_1x128_to_128x1(qx, sx, True)            # [C][T], [T/128][C]
+    qb, sb = F.quant_act_1x128(dy, False, transposed_input=True)  # [Co][T], [T/128][Co]
+    d = F.gemm_blockscaled(qa, sa, qb, sb, out_dtype=torch.float32, scale_b_1x128=True)
+    _full_check(d, qa, sa, qb, sb, "f32", "1x128")
+
+
+@pytest.mark.parametrize("K", [1024, 4096])
+def test_no_promotion_variant(F, K):
+    """Operands whose every 1x128 tile has the same power-of-two scale (2^-6):
+    the promoted and the tensor-core-only kernels see identical codes and
+    constant scales, so only the accumulation differs. Both are compared with
+    the exact result; the promoted one must meet the tolerance."""
+    M = N = 256
+    qa, sa = F.quant_act_1x128(W.ksweep_operand(M, K, 31).cuda(), True)
+    qb, sb = F.quant_act_1x128(W.ksweep_operand(N, K, 32).cuda(), True)
+    assert (sa == 2.0 ** -6).all() and (sb == 2.0 ** -6).all()
+    d_p = F.gemm_blockscaled(qa, sa, qb, sb, out_dtype=torch.float32, scale_b_1x128=True)
+    d_n = F.gemm_blockscaled(qa, sa, qb, sb, out_dtype=torch.float32, scale_b_1x128=True,
+                             no_promotion=True)
+    _full_check(d_p, qa, sa, qb, sb, "f32", "1x128")
+    ref = O.gemm_blockscaled(qa.cpu().numpy(), sa.cpu().numpy(), qb.cpu().numpy(),
+                             sb.cpu().numpy(), "1x128")
+    err_p = O.max_relative_error(to_np(d_p), ref)
+    err_n = O.max_relative_error(to_np(d_n), ref)
+    print(f"K={K}: max relative error promoted {err_p:.3e}, no promotion {err_n:.3e}")
+    assert err_n < 0.1  # same codes, only the accumulation differs
+
+
+# ------------------------------------------------- full-size workloads (bench sizes)
+def _sample_rows(M, n, seed):
+    g = np.random.default_rng(seed)
+    return np.unique(np.concatenate([g.choice(M, n, replace=False), [0, 127, 128, M - 1]]))
+
+
+def test_dense_forward_full_sampled(F):
+    """Dense forward [8192][7168] x [7168][7168] -> bf16, as timed by bench.py;
+    sampled rows x 128-column blocks against the oracle."""
+    p = W.DENSE_FWD
+    a, w = p.make()
+    qa, sa = F.quant_act_1x128(a.cuda())
+    qb, sb = F.quant_w_128x128(w.cuda())
+    d = F.gemm_blockscaled(qa, sa, qb, sb, out_dtype=torch.bfloat16)
+    check_gemm_sampled(to_np(d), qa.cpu().numpy(), sa.cpu().numpy(), qb.cpu().numpy(),
+                       sb.cpu().numpy(), _sample_rows(p.M, 40, 0), [0, 27, 55], "bf16")
+
+
+def test_square_8192_full_sampled(F):
+    p = W.SQUARE_8K
+    a, w = p.make()
+    qa, sa = F.quant_act_1x128(a.cuda())
+    qb, sb = F.quant_w_128x128(w.cuda())
+    d = F.gemm_blockscaled(qa, sa, qb, sb, out_dtype=torch.bfloat16)
+    check_gemm_sampled(to_np(d), qa.cpu().numpy(), sa.cpu().numpy(), qb.cpu().numpy(),
+                       sb.cpu().numpy(), _sample_rows(p.M, 40, 1), [0, 31, 63], "bf16")
+
+
+def test_wgrad_full_sampled(F):
+    """Wgrad: X [16384][7168] pow2 1x128 -> requant 128x1; dY [16384][7168]
+    ~N(0, 1e-6) 128x1 along tokens; dW = X^T dY in FP32, K = 16384."""
+    p = W.WgradProblem()
+    x, dy = p.make()
+    qx, sx = F.quant_act_1x128(x.cuda(), True)
+    qa, sa = F.requant_1x128_to_128x1(qx, sx, True)
+    del qx, sx
+    qb, sb = F.quant_act_1x128(dy.cuda(), False, transposed_input=True)
+    d = F.gemm_blockscaled(qa, sa, qb, sb, out_dtype=torch.float32, scale_b_1x128=True)
+    check_gemm_sampled(to_np(d), qa.cpu().numpy(), sa.cpu().numpy(), qb.cpu().numpy(),
+                       sb.cpu().numpy(), _sample_rows(p.C, 16, 2), [0, 55], "f32", "1x128")

@@ -1,0 +1,79 @@
+"""Grouped (MoE expert) GEMM on the GPU vs the per-expert oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle.fp8q_oracle as O
+from fp8_block_scaled_17_b300 import workloads as W
+from tests.helpers import assert_gemm_close, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def F(cuda_device):
+    from fp8_block_scaled_17_b300 import fp8q
+    return fp8q
+
+
+def _experts(F, E, K, N, seed):
+    w = torch.stack([W.bf16_normal((K, N), 0.02, seed + e) for e in range(E)]).cuda()
+    qb = torch.empty((E, N, K), dtype=torch.uint8, device="cuda")
+    sb = torch.empty((E, K // 128, N // 128), dtype=torch.float32, device="cuda")
+    for e in range(E):
+        F.quant_w_128x128(w[e], q=qb[e], sb=sb[e])
+    return qb, sb
+
+
+@pytest.mark.parametrize("sizes,out", [([3, 0, 1, 130, 0, 257], "f32"),
+                                       ([0, 0, 5], "bf16"),
+                                       ([128, 128, 1, 300], "bf16")])
+def test_grouped_small(F, sizes, out):
+    E, K, N = len(sizes), 384, 384
+    offs = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    Mtot = int(offs[-1])
+    x = W.bf16_normal((Mtot, K), 1.0, seed=sum(sizes), outlier_frac=0.002,
+                      outlier_scale=100.0).cuda()
+    qa, sa = F.quant_act_1x128(x, True)
+    qb, sb = _experts(F, E, K, N, seed=7)
+    dt = torch.bfloat16 if out == "bf16" else torch.float32
+    d = F.grouped_gemm(qa, sa, torch.from_numpy(offs).cuda(), qb, sb, out_dtype=dt)
+    assert F.get_status() == F.OK
+    qa_n, sa_n, qb_n, sb_n = (t.cpu().numpy() for t in (qa, sa, qb, sb))
+    ref = O.grouped_gemm_blockscaled(qa_n, sa_n, offs, qb_n, sb_n)
+    dn = to_np(d)
+    for e in range(E):
+        r0, r1 = offs[e], offs[e + 1]
+        if r1 > r0:
+            na, nb = O.row_col_norms(qa_n[r0:r1], sa_n[:, r0:r1], qb_n[e], sb_n[e])
+            assert_gemm_close(dn[r0:r1], ref[r0:r1], na, nb, out)
+
+
+def test_moe_full_sampled(F):
+    """16 experts, 16384 tokens x top-9 with Zipf(1.1) loads (147456 rows),
+    K = 7168, N = 2048, pow2 1x128 activation scales, bf16 out: the bench's
+    grouped workload. Sampled rows of every expert against the oracle."""
+    p = W.MoeProblem()
+    x, w, rows, offs = p.make()
+    qx, sx = F.quant_act_1x128(x.cuda(), True)            # quantize before dispatch
+    rows_d = rows.cuda()
+    qa = qx.index_select(0, rows_d).contiguous()          # dispatch: a row permutation
+    sa = sx.index_select(1, rows_d).contiguous()
+    qb = torch.empty((p.experts, p.N, p.K), dtype=torch.uint8, device="cuda")
+    sb = torch.empty((p.experts, p.K // 128, p.N // 128), dtype=torch.float32, device="cuda")
+    for e in range(p.experts):
+        F.quant_w_128x128(w[e].cuda(), q=qb[e], sb=sb[e])
+    d = F.grouped_gemm(qa, sa, offs.cuda(), qb, sb, out_dtype=torch.bfloat16)
+    assert F.get_status() == F.OK
+    dn = to_np(d)
+    qa_n, sa_n, qb_n, sb_n = (t.cpu().numpy() for t in (qa, sa, qb, sb))
+    o = offs.numpy()
+    g = np.random.default_rng(0)
+    cols = np.concatenate([np.arange(0, 128), np.arange(p.N - 128, p.N)])
+    for e in range(p.experts):
+        r0, r1 = int(o[e]), int(o[e + 1])
+        pick = np.unique(np.concatenate([g.integers(r0, r1, 6), [r0, r1 - 1]]))
+        sbe = sb_n[e][:, [0, p.N // 128 - 1]]
+        ref = O.gemm_blockscaled(qa_n[pick], sa_n[:, pick], qb_n[e][cols], sbe)
+        na, nb = O.row_col_norms(qa_n[pick], sa_n[:, pick], qb_n[e][cols], sbe)
+        assert_gemm_close(dn[np.ix_(pick, cols)], ref, na, nb, "bf16")

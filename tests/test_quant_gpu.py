@@ -1,0 +1,138 @@
+"""GPU quantizers vs the CPU oracle: codes and scales must match bit for bit."""
+import numpy as np
+import pytest
+import torch
+
+import oracle.fp8q_oracle as O
+from fp8_block_scaled_17_b300 import workloads as W
+from tests.helpers import bits
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def F(cuda_device):
+    from fp8_block_scaled_17_b300 import fp8q
+    return fp8q
+
+
+def _np(t):
+    return t.cpu().numpy()
+
+
+def _assert_same(q, s, rq, rs):
+    q, s = _np(q), _np(s)
+    assert q.shape == rq.shape and s.shape == rs.shape
+    bad = np.argwhere(q != rq)
+    assert bad.size == 0, f"{len(bad)} codes differ, first at {bad[0]}: {q[tuple(bad[0])]:#x} vs {rq[tuple(bad[0])]:#x}"
+    assert (bits(s) == bits(rs)).all(), "scales differ"
+
+
+# ------------------------------------------------------------- 1x128 rows
+@pytest.mark.parametrize("M,K,pow2", [(256, 512, False), (300, 1024, False), (300, 1024, True),
+                                      (1, 128, False), (65, 384, True), (4097, 256, False)])
+def test_quant_act_rows(F, M, K, pow2):
+    x = W.bf16_normal((M, K), 1.0, seed=M + K, outlier_frac=0.002, outlier_scale=100.0)
+    q, sa = F.quant_act_1x128(x.cuda(), pow2)
+    _assert_same(q, sa, *O.quant_act_1x128(x.float().numpy(), pow2))
+
+
+def test_quant_act_strided(F):
+    # x is a column slice of a wider matrix; codes land in a wider buffer
+    big = W.bf16_normal((70, 640), 1.0, seed=3)
+    x = big.cuda()[:, 128:512]
+    qbuf = torch.zeros((70, 512), dtype=torch.uint8, device="cuda")
+    q, sa = F.quant_act_1x128(x, False, q=qbuf[:, :384])
+    rq, rs = O.quant_act_1x128(big[:, 128:512].float().numpy(), False)
+    assert (_np(qbuf[:, :384]) == rq).all() and (_np(qbuf[:, 384:]) == 0).all()
+    assert (bits(_np(sa)) == bits(rs)).all()
+
+
+def _special_tiles():
+    mids = [(float(O._E4M3_NONNEG[c]) + float(O._E4M3_NONNEG[c + 1])) / 2 for c in range(126)]
+    rows = np.zeros((6, 128), np.float32)
+    # s = 56/448 = 2^-3 exactly: every other entry lands exactly on an E4M3 midpoint
+    rows[0, 0] = 56.0
+    rows[0, 1:127] = np.array(mids, np.float32) * np.float32(0.125)
+    rows[0, 127] = -rows[0, 64]
+    rows[1, :] = -rows[0, :]
+    rows[2, 5] = -0.0                       # all zero but one negative zero
+    rows[2, 9] = -0.0
+    rows[3, :] = np.float32(1e-40) * np.arange(-64, 64)   # bf16/f32 subnormals
+    rows[4, :] = np.linspace(-3.0e38, 3.0e38, 128)        # near the bf16 maximum
+    rows[5, ::2] = 1.0                      # amax 1.0 -> s = RN(1/448), quotient 448.00003
+    rows[5, 1::2] = -0.5
+    return torch.from_numpy(rows).to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("pow2", [False, True])
+def test_quant_act_special_values(F, pow2):
+    x = _special_tiles()
+    q, sa = F.quant_act_1x128(x.cuda(), pow2)
+    rq, rs = O.quant_act_1x128(x.float().numpy(), pow2)
+    _assert_same(q, sa, rq, rs)
+    if not pow2:  # the midpoint row really exercises ties-to-even
+        assert _np(q)[0, 0] == 0x7E and _np(q)[2, 5] == 0x80
+
+
+# ------------------------------------------------- 128x1 (transposed input)
+@pytest.mark.parametrize("K,M,pow2", [(256, 300, False), (512, 128, True), (384, 77, False)])
+def test_quant_act_transposed_input(F, K, M, pow2):
+    xt = W.bf16_normal((K, M), 1e-3, seed=K * M)   # stored [K][M], e.g. dY [tokens][channels]
+    q, s = F.quant_act_1x128(xt.cuda(), pow2, transposed_input=True)
+    _assert_same(q, s, *O.quant_act_1x128_transposed_input(xt.float().numpy(), pow2))
+
+
+# ---------------------------------------------------------------- 128x128
+@pytest.mark.parametrize("K,N,pow2", [(512, 256, False), (384, 640, True), (128, 128, False)])
+def test_quant_w(F, K, N, pow2):
+    w = W.bf16_normal((K, N), 0.02, seed=K + 7 * N, outlier_frac=0.001, outlier_scale=50.0)
+    q, sb = F.quant_w_128x128(w.cuda(), pow2)
+    _assert_same(q, sb, *O.quant_w_128x128(w.float().numpy(), pow2))
+
+
+# ----------------------------------------------------------- requant 1x128 -> 128x1
+@pytest.mark.parametrize("T,C,pow2", [(256, 384, True), (384, 256, False), (128, 128, True)])
+def test_requant(F, T, C, pow2):
+    x = W.bf16_normal((T, C), 1.0, seed=T * 3 + C, outlier_frac=0.003, outlier_scale=30.0)
+    qx, sx = F.quant_act_1x128(x.cuda(), pow2)
+    q2, s2 = F.requant_1x128_to_128x1(qx, sx, pow2)
+    rq, rs = O.quant_act_1x128(x.float().numpy(), pow2)
+    _assert_same(q2, s2, *O.requant_1x128_to_128x1(rq, rs, pow2))
+
+
+# ------------------------------------------------- full-size workloads (bench sizes)
+def test_quant_dense_forward_full(F):
+    """Dense forward activation [8192][7168] (0.1% x50 outliers) and weight
+    [7168][7168] ~ N(0, 0.02^2): every code and scale."""
+    a, w = W.DENSE_FWD.make()
+    qa, sa = F.quant_act_1x128(a.cuda())
+    _assert_same(qa, sa, *O.quant_act_1x128(a.float().numpy()))
+    qw, sw = F.quant_w_128x128(w.cuda())
+    _assert_same(qw, sw, *O.quant_w_128x128(w.float().numpy()))
+
+
+def test_quant_moe_and_wgrad_full_sampled(F):
+    """16384 x 7168 inputs of the MoE and Wgrad workloads: sampled row tiles of
+    the 1x128 quantizer, sampled channels of the 128x1 quantizer and of the
+    re-tiling."""
+    g = np.random.default_rng(0)
+    T, C = 16384, 7168
+    x = W.bf16_normal((T, C), 1.0, seed=0)
+    qx, sx = F.quant_act_1x128(x.cuda(), True)
+    rows = np.sort(np.concatenate([g.choice(T, 64, replace=False), [0, T - 1]]))
+    rq, rs = O.quant_act_1x128(x[rows].float().numpy(), True)
+    assert (_np(qx)[rows] == rq).all() and (bits(_np(sx)[:, rows]) == bits(rs)).all()
+
+    q2, s2 = F.requant_1x128_to_128x1(qx, sx, True)
+    qxn, sxn, q2n, s2n = _np(qx), _np(sx), _np(q2), _np(s2)
+    for cb in (0, 17, C // 128 - 1):  # whole 128-channel blocks (all tokens)
+        cs = slice(cb * 128, (cb + 1) * 128)
+        rq2, rs2 = O.requant_1x128_to_128x1(qxn[:, cs], sxn[cb:cb + 1, :], True)
+        assert (q2n[cs] == rq2).all() and (bits(s2n[:, cs]) == bits(rs2)).all()
+
+    chans = np.sort(np.concatenate([g.choice(C, 24, replace=False), [0, C - 1]]))
+    dy = W.bf16_normal((T, C), 1e-3, seed=1)
+    qd, sd = F.quant_act_1x128(dy.cuda(), False, transposed_input=True)
+    rq3, rs3 = O.quant_act_1x128(dy[:, chans].float().numpy().T, False)
+    assert (_np(qd)[chans] == rq3).all() and (bits(_np(sd)[:, chans]) == bits(rs3)).all()
