@@ -79,7 +79,10 @@ def test_quant_act_special_values(F, pow2):
 @pytest.mark.parametrize("K,M,pow2", [(256, 300, False), (512, 128, True), (384, 77, False)])
 def test_quant_act_transposed_input(F, K, M, pow2):
     xt = W.bf16_normal((K, M), 1e-3, seed=K * M)   # stored [K][M], e.g. dY [tokens][channels]
-    q, s = F.quant_act_1x128(xt.cuda(), pow2, transposed_input=True)
+    ld = -(-M // 8) * 8                            # rows padded to 16 bytes
+    buf = torch.zeros((K, ld), dtype=torch.bfloat16, device="cuda")
+    buf[:, :M] = xt.cuda()
+    q, s = F.quant_act_1x128(buf[:, :M], pow2, transposed_input=True)
     _assert_same(q, s, *O.quant_act_1x128_transposed_input(xt.float().numpy(), pow2))
 
 
