@@ -28,7 +28,8 @@ constexpr uint64_t kWaitLimitNs = 4000000000ull;  // 4 s: far above any legal wa
 struct DeviceInfo {
   bool ready = false;
   bool supported = false;
-  bool gemm_ok = false;  // the GEMM's register split matches its compiled count
+  bool gemm_ok = false;     // BN = 128 GEMM can be launched with 384 threads
+  bool gemm256_ok = false;  // BN = 256: its register split matches the compiled count
   int num_sms = 0;
   unsigned* status = nullptr;
 };
@@ -50,17 +51,23 @@ fp8q_status device_info(DeviceInfo** out) {
     d.supported = (prop.major == 10 && prop.minor == 3);
     d.num_sms = prop.multiProcessorCount;
     if (d.supported) {
-      const int smem = static_cast<int>(fp8q::gemm::Layout::bytes(fp8q::gemm::kMaxExperts));
-      if (cudaFuncSetAttribute(fp8q::gemm::gemm_blockscaled_kernel,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+      using namespace fp8q::gemm;
+      const int smem128 = static_cast<int>(Cfg<128>::bytes(kMaxExperts));
+      const int smem256 = static_cast<int>(Cfg<256>::bytes(kMaxExperts));
+      if (cudaFuncSetAttribute(gemm_blockscaled_kernel<128>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, smem128) != cudaSuccess ||
+          cudaFuncSetAttribute(gemm_blockscaled_kernel<256>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, smem256) != cudaSuccess)
         return FP8Q_ERR_CUDA;
-      // setmaxnreg.inc can only hand out what the block was launched with: a
-      // split that exceeds it would wait forever, so check before any launch.
-      cudaFuncAttributes fa;
-      if (cudaFuncGetAttributes(&fa, fp8q::gemm::gemm_blockscaled_kernel) != cudaSuccess)
+      // setmaxnreg.inc (BN = 256) can only hand out what the block was launched
+      // with: a split that exceeds it would wait forever, so check the compiled
+      // register count before any launch.
+      cudaFuncAttributes fa128, fa256;
+      if (cudaFuncGetAttributes(&fa128, gemm_blockscaled_kernel<128>) != cudaSuccess ||
+          cudaFuncGetAttributes(&fa256, gemm_blockscaled_kernel<256>) != cudaSuccess)
         return FP8Q_ERR_CUDA;
-      d.gemm_ok = fa.numRegs == fp8q::gemm::kLaunchRegs &&
-                  fa.maxThreadsPerBlock >= fp8q::gemm::kThreads;
+      d.gemm_ok = fa128.maxThreadsPerBlock >= kThreads;
+      d.gemm256_ok = fa256.numRegs == kLaunchRegs && fa256.maxThreadsPerBlock >= kThreads;
       void* addr = nullptr;
       if (cudaGetSymbolAddress(&addr, g_device_status) != cudaSuccess) return FP8Q_ERR_CUDA;
       d.status = static_cast<unsigned*>(addr);
@@ -132,11 +139,14 @@ fp8q_status gemm_common(const uint8_t* A, const float* sa, const int32_t* m_offs
 
   DeviceInfo* dev = nullptr;
   if (fp8q_status st = device_info(&dev)) return st;
-  if (!dev->gemm_ok) return FP8Q_ERR_UNSUPPORTED;
+  // CTA tile N: 256 (two TMEM accumulator buffers) unless FP8Q_GEMM_TILE_N=128
+  const char* tn = std::getenv("FP8Q_GEMM_TILE_N");
+  const int bn = (tn && std::strcmp(tn, "128") == 0) ? 128 : 256;
+  if (bn == 128 ? !dev->gemm_ok : !dev->gemm256_ok) return FP8Q_ERR_UNSUPPORTED;
 
   const uint32_t box_a_rows = static_cast<uint32_t>(M < BM ? M : BM);
   const int64_t b_rows = static_cast<int64_t>(E) * N;
-  const uint32_t box_b_rows = static_cast<uint32_t>(b_rows < BN ? b_rows : BN);
+  const uint32_t box_b_rows = static_cast<uint32_t>(b_rows < bn ? b_rows : bn);
   CUtensorMap tmA, tmB;
   if (!encode_u8_2d(&tmA, A, K, M, K, BK, box_a_rows)) return FP8Q_ERR_CUDA;
   if (!encode_u8_2d(&tmB, B, K, b_rows, K, BK, box_b_rows)) return FP8Q_ERR_CUDA;
@@ -162,11 +172,14 @@ fp8q_status gemm_common(const uint8_t* A, const float* sa, const int32_t* m_offs
 
   int grid = dev->num_sms;
   if (!grouped) {
-    const int64_t tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+    const int64_t tiles = ((M + BM - 1) / BM) * ((N + bn - 1) / bn);
     if (tiles < grid) grid = static_cast<int>(tiles);
   }
-  const size_t smem = Layout::bytes(E);
-  gemm_blockscaled_kernel<<<grid, kThreads, smem, stream>>>(tmA, tmB, p);
+  if (bn == 128) {
+    gemm_blockscaled_kernel<128><<<grid, kThreads, Cfg<128>::bytes(E), stream>>>(tmA, tmB, p);
+  } else {
+    gemm_blockscaled_kernel<256><<<grid, kThreads, Cfg<256>::bytes(E), stream>>>(tmA, tmB, p);
+  }
   return launch_status();
 }
 

@@ -5,24 +5,27 @@
 // are multiplied in there; "Don't Be Fooled By Deepseek Chatgpt", Figure 7 (b)).
 //
 // The pages describe two Hopper warpgroups whose WGMMA and promotion overlap.
-// On sm_103a the same overlap comes from tensor memory: the MMA of chunk kb+1
-// runs into one TMEM buffer while the promotion warps drain chunk kb from the
-// other.
+// On sm_103a the same overlap comes from tensor memory: the MMAs of the next
+// chunks run into other TMEM buffers while the promotion warps drain chunk kb.
 //
-// CTA tile 128 (M) x 256 (N); one 128-K chunk = 4 tcgen05.mma (K = 32 each).
+// CTA tile 128 (M) x BN (N), BN = 128 or 256; one 128-K chunk = 4
+// tcgen05.mma (K = 32 each) into one TMEM accumulator buffer of BN columns.
+// TMEM (512 columns) holds 512/BN buffers: 4 for BN = 128, so the promotion of
+// a chunk may take up to three chunks of MMA time before the buffer it reads
+// is needed again.
 // Warp roles (384 threads = 3 warpgroups, one CTA per SM, persistent over tiles):
 //   warps 0-7  promotion + epilogue. Warp w reads TMEM lanes 32*(w%4).. (rows)
-//              and columns 128*(w/4).. of the tile: each thread owns one row and
-//              128 FP32 accumulators in registers. Per chunk it loads P_kb from
-//              TMEM and does acc += P_kb * (sa[kb][m] * sb[kb][n/128]).
-//   warp 8     TMA producer: A (128 x 128 B) and B (256 x 128 B) tiles into a
-//              4-stage shared-memory ring, 128-byte swizzled.
+//              and columns (BN/2)*(w/4).. of the tile: each thread owns one row
+//              and BN/2 FP32 accumulators in registers. Per chunk it loads P_kb
+//              from TMEM and does acc += P_kb * (sa[kb][m] * sb[kb][n/128]).
+//   warp 8     TMA producer: A (128 x 128 B) and B (BN x 128 B) tiles into a
+//              shared-memory ring, 128-byte swizzled.
 //   warp 9     TMEM allocator + MMA issuer (one thread).
 //   warps 10-11 idle (they complete the third warpgroup).
-// Register split (setmaxnreg): the kernel is launched with 168 registers per
-// thread (384 x 168 = 64512); the producer/MMA warpgroup gives up to 40 and the
-// two promotion warpgroups rise to 232 (128 x 40 + 256 x 232 = 64512). The
-// host refuses to launch unless the compiled count is exactly kLaunchRegs.
+// BN = 256 needs 128 accumulators + 64 staging registers per promotion thread:
+// the kernel is launched with 168 registers per thread (384 x 168 = 64512) and
+// setmaxnreg moves them (128 x 40 + 256 x 232 = 64512). The host refuses to
+// launch unless the compiled count is exactly kLaunchRegs.
 // Scales reach the promotion warps through a per-warp shared-memory ring fed
 // by cp.async three chunks ahead.
 //
@@ -45,10 +48,8 @@ constexpr unsigned kDevStatusBadOffsets = 2u;
 
 namespace gemm {
 
-constexpr int BM = 128, BN = 256, BK = 128;
-constexpr int kStages = 4;
+constexpr int BM = 128, BK = 128;
 constexpr int kABytes = BM * BK;  // 16 KB
-constexpr int kBBytes = BN * BK;  // 32 KB
 constexpr int kPromoWarps = 8;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
@@ -60,13 +61,33 @@ static_assert(kThreads * kLaunchRegs >= 256 * kPromoRegs + 128 * kCtrlRegs,
               "register split exceeds the launch budget");
 constexpr int kScaleSlots = 4;  // per promotion warp
 constexpr int kScaleAhead = 3;  // chunks of scales in flight
-constexpr int kSlotFloats = 32 + 128;
-constexpr uint32_t kTmemCols = 512;  // two 256-column accumulator buffers
+constexpr uint32_t kTmemCols = 512;
 constexpr int kMaxExperts = 1024;
 
 constexpr int kFlagPromote = 1;
 constexpr int kFlagOutBF16 = 2;
 constexpr int kFlagScaleB1x128 = 4;
+
+template <int BN>
+struct Cfg {
+  static constexpr int kBBytes = BN * BK;
+  static constexpr int kStages = BN == 256 ? 4 : 6;
+  static constexpr int kAccBufs = 512 / BN;
+  static constexpr int kWarpCols = BN / 2;  // accumulator columns per promotion thread
+  static constexpr int kSlotFloats = 32 + kWarpCols;
+  static constexpr bool kSplitRegs = BN == 256;
+  // shared memory layout (offsets from a 1024-byte aligned base)
+  static constexpr uint32_t a_off = 0;
+  static constexpr uint32_t b_off = a_off + kStages * kABytes;
+  static constexpr uint32_t scale_off = b_off + kStages * kBBytes;
+  static constexpr uint32_t scale_bytes = kPromoWarps * kScaleSlots * kSlotFloats * 4;
+  static constexpr uint32_t bar_off = scale_off + scale_bytes;
+  static constexpr uint32_t n_bars = 2 * kStages + 2 * kAccBufs + 2;
+  static constexpr uint32_t misc_off = bar_off + n_bars * 8;  // tmem base, abort flag
+  static constexpr uint32_t table_off = misc_off + 16;        // seg[E+1], prefix[E+1]
+  static constexpr uint32_t bytes(int E) { return table_off + 8u * (E + 1) + 1024u; }
+  static_assert(bytes(kMaxExperts) <= 232448, "shared memory budget");
+};
 
 struct Params {
   const float* sa;            // [K/128][M]
@@ -84,18 +105,6 @@ struct Params {
   int inject_timeout;
 };
 
-struct Layout {
-  static constexpr uint32_t a_off = 0;
-  static constexpr uint32_t b_off = a_off + kStages * kABytes;
-  static constexpr uint32_t scale_off = b_off + kStages * kBBytes;
-  static constexpr uint32_t scale_bytes = kPromoWarps * kScaleSlots * kSlotFloats * 4;
-  static constexpr uint32_t bar_off = scale_off + scale_bytes;
-  static constexpr uint32_t n_bars = 2 * kStages + 6;
-  static constexpr uint32_t misc_off = bar_off + n_bars * 8;  // tmem base, abort flag
-  static constexpr uint32_t table_off = misc_off + 16;        // seg[E+1], prefix[E+1]
-  static constexpr uint32_t bytes(int E) { return table_off + 8u * (E + 1) + 1024u; }
-};
-
 struct Tile {
   int64_t m0;     // first row of A (and D)
   int64_t m_end;  // rows >= m_end belong to another expert / are padding
@@ -108,7 +117,7 @@ struct Tile {
 // groups of group_m M-tiles, N fastest inside a group column, so that the CTAs
 // running at the same time share A rows and B columns in L2.
 __device__ __forceinline__ Tile tile_at(int t, const int* seg, const int* pre, int E, int nt,
-                                        int N, int group_m) {
+                                        int N, int group_m, int bn) {
   int lo = 0, hi = E;  // pre[lo] <= t < pre[hi]
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
@@ -127,7 +136,7 @@ __device__ __forceinline__ Tile tile_at(int t, const int* seg, const int* pre, i
   tl.e = e;
   tl.m0 = static_cast<int64_t>(seg[e]) + static_cast<int64_t>(first + r % gs) * BM;
   tl.m_end = seg[e + 1];
-  tl.n0 = (r / gs) * BN;
+  tl.n0 = (r / gs) * bn;
   tl.brow0 = e * N + tl.n0;
   return tl;
 }
@@ -163,31 +172,59 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
-// Position of the promotion warp's scale prefetch in its (tile, unit) stream.
+// a += b * c on two float32 lanes at once (each lane one fused multiply-add,
+// rounded once, as fmaf).
+__device__ __forceinline__ void ffma2(float& a0, float& a1, float b0, float b1, float c0,
+                                      float c1) {
+  asm("{\n\t.reg .b64 ra, rb, rc;\n\t"
+      "mov.b64 ra, {%0, %1};\n\tmov.b64 rb, {%2, %3};\n\tmov.b64 rc, {%4, %5};\n\t"
+      "fma.rn.f32x2 ra, rb, rc, ra;\n\tmov.b64 {%0, %1}, ra;\n\t}"
+      : "+f"(a0), "+f"(a1)
+      : "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+// d = a * b on two lanes (each rounded once, as __fmul_rn).
+__device__ __forceinline__ void fmul2(float& d0, float& d1, float a0, float a1, float b0,
+                                      float b1) {
+  asm("{\n\t.reg .b64 rd, ra, rb;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
+// Position of a promotion warp's scale prefetch in its (tile, unit) stream,
+// with the tile it last looked up.
 struct ScaleStream {
   int t;       // tile
   int u;       // unit (K-block, or 0 without promotion)
   uint32_t n;  // units issued so far (ring slot = n % kScaleSlots)
+  int cached_t;
+  Tile tl;
 };
 
 // Copy (cp.async) the scales one promotion warp needs for the next unit of its
 // stream into its ring slot: sa of its 32 rows, and either the one 128x128
-// B-block scale of its column half or 128 per-column B scales. One commit
-// group per unit (empty past the last tile, so that group counting stays
-// uniform).
+// B-block scale of its columns or their per-column B scales. One commit group
+// per unit (empty past the last tile, so that group counting stays uniform).
+template <int BN>
 __device__ __forceinline__ void issue_scales(ScaleStream& ss, const Params& p, const int* seg,
                                              const int* pre, int nt, int KB, int NB, int units,
                                              int total, bool promote, bool sb1, int q, int h,
                                              int lane, uint32_t ring_s) {
-  const uint32_t dst = ring_s + (ss.n % kScaleSlots) * (kSlotFloats * 4);
+  using C = Cfg<BN>;
+  const uint32_t dst = ring_s + (ss.n % kScaleSlots) * (C::kSlotFloats * 4);
   if (ss.t < total) {
-    const Tile tl = tile_at(ss.t, seg, pre, p.E, nt, p.N, p.group_m);
+    if (ss.t != ss.cached_t) {
+      ss.tl = tile_at(ss.t, seg, pre, p.E, nt, p.N, p.group_m, BN);
+      ss.cached_t = ss.t;
+    }
+    const Tile& tl = ss.tl;
     const int kb = promote ? ss.u : 0;
     const int64_t m = tl.m0 + q * 32 + lane;
     const bool rok = m < tl.m_end;
     cp_async_4(dst + 4u * lane, p.sa + static_cast<int64_t>(kb) * p.M + (rok ? m : 0),
                rok ? 4u : 0u);
-    const int col0 = tl.n0 + h * 128;
+    const int col0 = tl.n0 + h * C::kWarpCols;
     const bool cok = col0 < p.N;
     if (!sb1) {
       if (lane == 0) {
@@ -195,7 +232,7 @@ __device__ __forceinline__ void issue_scales(ScaleStream& ss, const Params& p, c
             p.sb + (static_cast<int64_t>(tl.e) * KB + kb) * NB + (cok ? col0 / 128 : 0);
         cp_async_4(dst + 4u * 32, src, cok ? 4u : 0u);
       }
-    } else {
+    } else if (lane < C::kWarpCols / 4) {
       const float* src = p.sb + static_cast<int64_t>(kb) * p.N + (cok ? col0 + 4 * lane : 0);
       cp_async_16(dst + 4u * (32 + 4 * lane), src, cok ? 16u : 0u);
     }
@@ -208,9 +245,15 @@ __device__ __forceinline__ void issue_scales(ScaleStream& ss, const Params& p, c
   }
 }
 
+template <int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_blockscaled_kernel(const __grid_constant__ CUtensorMap tmA,
                             const __grid_constant__ CUtensorMap tmB, const Params p) {
+  using C = Cfg<BN>;
+  constexpr int kStages = C::kStages;
+  constexpr int kAccBufs = C::kAccBufs;
+  constexpr int kWarpCols = C::kWarpCols;
+
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -218,16 +261,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  const uint32_t bar0 = base + Layout::bar_off;
+  const uint32_t bar0 = base + C::bar_off;
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (kStages + s); };
   auto tfull_bar = [&](uint32_t b) { return bar0 + 8u * (2 * kStages + b); };
-  auto tempty_bar = [&](uint32_t b) { return bar0 + 8u * (2 * kStages + 2 + b); };
-  const uint32_t drain_bar = bar0 + 8u * (2 * kStages + 4);
-  const uint32_t never_bar = bar0 + 8u * (2 * kStages + 5);
-  uint32_t* const misc = reinterpret_cast<uint32_t*>(base_ptr + Layout::misc_off);
+  auto tempty_bar = [&](uint32_t b) { return bar0 + 8u * (2 * kStages + kAccBufs + b); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * kStages + 2 * kAccBufs);
+  const uint32_t never_bar = drain_bar + 8u;
+  uint32_t* const misc = reinterpret_cast<uint32_t*>(base_ptr + C::misc_off);
   volatile uint32_t* const abort_flag = misc + 1;
-  int* const seg = reinterpret_cast<int*>(base_ptr + Layout::table_off);
+  int* const seg = reinterpret_cast<int*>(base_ptr + C::table_off);
   int* const pre = seg + (p.E + 1);
 
   const int nt = (p.N + BN - 1) / BN;
@@ -239,7 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     seg[e] = p.m_offsets ? __ldg(p.m_offsets + e) : (e == 0 ? 0 : static_cast<int>(p.M));
   }
   if (warp == kMmaWarp) {
-    tmem_alloc(base + Layout::misc_off, kTmemCols);
+    tmem_alloc(base + C::misc_off, kTmemCols);
     tmem_relinquish();
   }
   if (threadIdx.x == 0) {
@@ -247,7 +290,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);
     }
-    for (uint32_t b = 0; b < 2; ++b) {
+    for (uint32_t b = 0; b < kAccBufs; ++b) {
       mbar_init(tfull_bar(b), 1);
       mbar_init(tempty_bar(b), kPromoWarps);
     }
@@ -287,173 +330,184 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int total = pre[p.E];
 
   if (warp >= kPromoWarps) {
-  setmaxnreg_dec<kCtrlRegs>();
-  if (warp == kProducerWarp) {
-    // ------------------------------------------------------- TMA producer
-    if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      int issued = 0;
-      bool ok = true;
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        const Tile tl = tile_at(t, seg, pre, p.E, nt, p.N, p.group_m);
-        for (int kb = 0; kb < KB; ++kb) {
-          if (!wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, p, p.wait_limit_ns)) {
-            ok = false;
-            break;
+    if constexpr (C::kSplitRegs) setmaxnreg_dec<kCtrlRegs>();
+    if (warp == kProducerWarp) {
+      // ----------------------------------------------------- TMA producer
+      if (lane == 0) {
+        int stage = 0;
+        uint32_t phase = 0;
+        int issued = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+          const Tile tl = tile_at(t, seg, pre, p.E, nt, p.N, p.group_m, BN);
+          for (int kb = 0; kb < KB; ++kb) {
+            if (!wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, p, p.wait_limit_ns)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(full_bar(stage), p.tx_bytes);
+            tma_load_2d(base + C::a_off + stage * kABytes, &tmA, full_bar(stage), kb * BK,
+                        static_cast<int32_t>(tl.m0));
+            tma_load_2d(base + C::b_off + stage * C::kBBytes, &tmB, full_bar(stage), kb * BK,
+                        tl.brow0);
+            ++issued;
+            if (++stage == kStages) { stage = 0; phase ^= 1u; }
           }
-          mbar_arrive_expect_tx(full_bar(stage), p.tx_bytes);
-          tma_load_2d(base + Layout::a_off + stage * kABytes, &tmA, full_bar(stage), kb * BK,
-                      static_cast<int32_t>(tl.m0));
-          tma_load_2d(base + Layout::b_off + stage * kBBytes, &tmB, full_bar(stage), kb * BK,
-                      tl.brow0);
-          ++issued;
-          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) {  // let the loads still in flight land before the CTA exits
+          const int n = issued < kStages ? issued : kStages;
+          for (int i = 1; i <= n; ++i) {
+            int s = stage - i;
+            uint32_t ph = phase;
+            if (s < 0) { s += kStages; ph ^= 1u; }
+            wait_drain(full_bar(s), ph, p.wait_limit_ns);
+          }
         }
       }
-      if (!ok) {  // let the loads still in flight land before the CTA exits
-        const int n = issued < kStages ? issued : kStages;
-        for (int i = 1; i <= n; ++i) {
-          int s = stage - i;
-          uint32_t ph = phase;
-          if (s < 0) { s += kStages; ph ^= 1u; }
-          wait_drain(full_bar(s), ph, p.wait_limit_ns);
-        }
-      }
-    }
-    __syncwarp();
-  } else if (warp == kMmaWarp) {
-    // ----------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc = idesc_e4m3_f32(BM, BN);
-      int stage = 0;
-      uint32_t phase = 0;
-      uint32_t unit = 0;
-      bool ok = true;
-      if (p.inject_timeout) ok = wait_bounded(never_bar, 0u, abort_flag, p, 20000000ull);
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        for (int kb = 0; kb < KB; ++kb) {
-          const uint32_t b = unit & 1u;
-          if (promote || kb == 0) {
-            if (!wait_bounded(tempty_bar(b), ((unit >> 1) & 1u) ^ 1u, abort_flag, p,
-                              p.wait_limit_ns)) {
+      __syncwarp();
+    } else if (warp == kMmaWarp) {
+      // --------------------------------------------------------- MMA issuer
+      if (lane == 0) {
+        constexpr uint32_t idesc = idesc_e4m3_f32(BM, BN);
+        int stage = 0;
+        uint32_t phase = 0;
+        uint32_t unit = 0;  // accumulation units issued (one per chunk, or per tile)
+        bool ok = true;
+        if (p.inject_timeout) ok = wait_bounded(never_bar, 0u, abort_flag, p, 20000000ull);
+        for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+          for (int kb = 0; kb < KB; ++kb) {
+            const uint32_t b = unit % kAccBufs;
+            if (promote || kb == 0) {
+              if (!wait_bounded(tempty_bar(b), ((unit / kAccBufs) & 1u) ^ 1u, abort_flag, p,
+                                p.wait_limit_ns)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+            }
+            if (!wait_bounded(full_bar(stage), phase, abort_flag, p, p.wait_limit_ns)) {
               ok = false;
               break;
             }
             tc_fence_after();
-          }
-          if (!wait_bounded(full_bar(stage), phase, abort_flag, p, p.wait_limit_ns)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint64_t adesc = sw128_kmajor_desc(base + Layout::a_off + stage * kABytes);
-          const uint64_t bdesc = sw128_kmajor_desc(base + Layout::b_off + stage * kBBytes);
-          const uint32_t d_tmem = tmem_base + b * BN;
+            const uint64_t adesc = sw128_kmajor_desc(base + C::a_off + stage * kABytes);
+            const uint64_t bdesc = sw128_kmajor_desc(base + C::b_off + stage * C::kBBytes);
+            const uint32_t d_tmem = tmem_base + b * BN;
 #pragma unroll
-          for (int k = 0; k < BK / 32; ++k) {
-            // advance 32 bytes of K inside the swizzled 128-byte rows
-            umma_f8f6f4(d_tmem, adesc + 2u * k, bdesc + 2u * k, idesc,
-                        (k > 0 || (!promote && kb > 0)) ? 1u : 0u);
+            for (int k = 0; k < BK / 32; ++k) {
+              // advance 32 bytes of K inside the swizzled 128-byte rows
+              umma_f8f6f4(d_tmem, adesc + 2u * k, bdesc + 2u * k, idesc,
+                          (k > 0 || (!promote && kb > 0)) ? 1u : 0u);
+            }
+            umma_commit(empty_bar(stage));
+            if (promote || kb == KB - 1) {
+              umma_commit(tfull_bar(b));
+              ++unit;
+            }
+            if (++stage == kStages) { stage = 0; phase ^= 1u; }
           }
-          umma_commit(empty_bar(stage));
-          if (promote || kb == KB - 1) {
-            umma_commit(tfull_bar(b));
-            ++unit;
-          }
-          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) {  // wait for the MMAs already issued
+          umma_commit(drain_bar);
+          wait_drain(drain_bar, 0u, p.wait_limit_ns);
         }
       }
-      if (!ok) {  // wait for the MMAs already issued
-        umma_commit(drain_bar);
-        wait_drain(drain_bar, 0u, p.wait_limit_ns);
-      }
+      __syncwarp();
     }
-    __syncwarp();
-  }
   } else {
-    setmaxnreg_inc<kPromoRegs>();
-    // ------------------------------------------------- promotion + epilogue
+    if constexpr (C::kSplitRegs) setmaxnreg_inc<kPromoRegs>();
+    // --------------------------------------------------- promotion + epilogue
     const int q = warp & 3;   // TMEM lane quarter -> rows 32q .. 32q+31
-    const int h = warp >> 2;  // column half -> columns 128h .. 128h+127
+    const int h = warp >> 2;  // column half -> columns h*BN/2 ..
     const bool sb1 = (p.flags & kFlagScaleB1x128) != 0;
     const int NB = (p.N + 127) / 128;
     const int units = promote ? KB : 1;
-    const float* const ring = reinterpret_cast<const float*>(base_ptr + Layout::scale_off) +
-                              warp * kScaleSlots * kSlotFloats;
-    const uint32_t ring_s = base + Layout::scale_off + warp * kScaleSlots * kSlotFloats * 4;
+    const float* const ring = reinterpret_cast<const float*>(base_ptr + C::scale_off) +
+                              warp * kScaleSlots * C::kSlotFloats;
+    const uint32_t ring_s = base + C::scale_off + warp * kScaleSlots * C::kSlotFloats * 4;
 
-    // scale prefetch stream over (tile, unit)
-    ScaleStream ss{static_cast<int>(blockIdx.x), 0, 0u};
+    ScaleStream ss;
+    ss.t = blockIdx.x;
+    ss.u = 0;
+    ss.n = 0u;
+    ss.cached_t = -1;
     for (int i = 0; i < kScaleAhead; ++i)
-      issue_scales(ss, p, seg, pre, nt, KB, NB, units, total, promote, sb1, q, h, lane, ring_s);
+      issue_scales<BN>(ss, p, seg, pre, nt, KB, NB, units, total, promote, sb1, q, h, lane,
+                       ring_s);
 
     uint32_t unit = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-      const Tile tl = tile_at(t, seg, pre, p.E, nt, p.N, p.group_m);
-      float acc[128];
+      const Tile tl = tile_at(t, seg, pre, p.E, nt, p.N, p.group_m, BN);
+      float acc[kWarpCols];
 #pragma unroll
-      for (int j = 0; j < 128; ++j) acc[j] = 0.0f;
+      for (int j = 0; j < kWarpCols; ++j) acc[j] = 0.0f;
 
       for (int u = 0; u < units; ++u) {
         cp_async_wait<kScaleAhead - 1>();
         __syncwarp();
-        const float* slot = ring + (unit % kScaleSlots) * kSlotFloats;
+        const float* slot = ring + (unit % kScaleSlots) * C::kSlotFloats;
         const float sa_v = slot[lane];
-        const uint32_t b = unit & 1u;
+        const uint32_t b = unit % kAccBufs;
         // every lane waits; the vote keeps the warp-collective TMEM loads uniform
-        const bool got = wait_bounded(tfull_bar(b), (unit >> 1) & 1u, abort_flag, p,
+        const bool got = wait_bounded(tfull_bar(b), (unit / kAccBufs) & 1u, abort_flag, p,
                                       p.wait_limit_ns);
         if (!__all_sync(0xffffffffu, got)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + b * BN + h * 128;
+        const uint32_t taddr =
+            tmem_base + (static_cast<uint32_t>(q * 32) << 16) + b * BN + h * kWarpCols;
         const float s_blk = sb1 ? 0.0f : __fmul_rn(sa_v, slot[32]);
+        constexpr int kRounds = kWarpCols / 64;
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
+        for (int rd = 0; rd < kRounds; ++rd) {
           uint32_t r0[32], r1[32];
-          tmem_ld_32x32b_x32(taddr + half * 64, r0);
-          tmem_ld_32x32b_x32(taddr + half * 64 + 32, r1);
+          tmem_ld_32x32b_x32(taddr + rd * 64, r0);
+          tmem_ld_32x32b_x32(taddr + rd * 64 + 32, r1);
           tmem_ld_wait();
-          if (half == 1) {  // buffer fully read: hand it back to the MMA issuer
+          if (rd == kRounds - 1) {  // buffer fully read: hand it back to the MMA issuer
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(tempty_bar(b));
           }
+          float* a = acc + rd * 64;
           if (!sb1) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              acc[half * 64 + j] = fmaf(__uint_as_float(r0[j]), s_blk, acc[half * 64 + j]);
-              acc[half * 64 + 32 + j] =
-                  fmaf(__uint_as_float(r1[j]), s_blk, acc[half * 64 + 32 + j]);
+            for (int j = 0; j < 32; j += 2) {
+              ffma2(a[j], a[j + 1], __uint_as_float(r0[j]), __uint_as_float(r0[j + 1]), s_blk,
+                    s_blk);
+              ffma2(a[32 + j], a[33 + j], __uint_as_float(r1[j]), __uint_as_float(r1[j + 1]),
+                    s_blk, s_blk);
             }
           } else {
+            const float* sbv = slot + 32 + rd * 64;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const float s0 = __fmul_rn(sa_v, slot[32 + half * 64 + j]);
-              const float s1 = __fmul_rn(sa_v, slot[32 + half * 64 + 32 + j]);
-              acc[half * 64 + j] = fmaf(__uint_as_float(r0[j]), s0, acc[half * 64 + j]);
-              acc[half * 64 + 32 + j] =
-                  fmaf(__uint_as_float(r1[j]), s1, acc[half * 64 + 32 + j]);
+            for (int j = 0; j < 32; j += 2) {
+              float c0, c1, c2, c3;
+              fmul2(c0, c1, sa_v, sa_v, sbv[j], sbv[j + 1]);
+              fmul2(c2, c3, sa_v, sa_v, sbv[32 + j], sbv[33 + j]);
+              ffma2(a[j], a[j + 1], __uint_as_float(r0[j]), __uint_as_float(r0[j + 1]), c0, c1);
+              ffma2(a[32 + j], a[33 + j], __uint_as_float(r1[j]), __uint_as_float(r1[j + 1]),
+                    c2, c3);
             }
           }
         }
         ++unit;
-        issue_scales(ss, p, seg, pre, nt, KB, NB, units, total, promote, sb1, q, h, lane, ring_s);
+        issue_scales<BN>(ss, p, seg, pre, nt, KB, NB, units, total, promote, sb1, q, h, lane,
+                         ring_s);
       }
       if (!ok) break;
 
       // ---------------------------------------------------------- epilogue
       const int64_t m = tl.m0 + q * 32 + lane;
-      const int col0 = tl.n0 + h * 128;
+      const int col0 = tl.n0 + h * kWarpCols;
       if (m < tl.m_end && col0 < p.N) {
         if (p.flags & kFlagOutBF16) {
           uint4* d = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.D) + m * p.ldd + col0);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
+          for (int j = 0; j < kWarpCols / 8; ++j) {
             d[j] = make_uint4(pack_bf16x2(acc[8 * j + 0], acc[8 * j + 1]),
                               pack_bf16x2(acc[8 * j + 2], acc[8 * j + 3]),
                               pack_bf16x2(acc[8 * j + 4], acc[8 * j + 5]),
@@ -462,7 +516,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
           float4* d = reinterpret_cast<float4*>(static_cast<float*>(p.D) + m * p.ldd + col0);
 #pragma unroll
-          for (int j = 0; j < 32; ++j)
+          for (int j = 0; j < kWarpCols / 4; ++j)
             d[j] = make_float4(acc[4 * j], acc[4 * j + 1], acc[4 * j + 2], acc[4 * j + 3]);
         }
       }

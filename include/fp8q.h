@@ -159,6 +159,8 @@ fp8q_status fp8q_grouped_gemm(const uint8_t* A, const float* sa, const int32_t* 
  * usable), FP8Q_ERR_INVALID_ARG for malformed grouped-GEMM offsets,
  * FP8Q_ERR_CUDA if the stream reported a CUDA error. No counterpart in the
  * pages: this is the library's failure-detection hook.
+ * Tuning: FP8Q_GEMM_TILE_N=128 selects 128x128 CTA tiles (four TMEM
+ * accumulator buffers) instead of the default 128x256 (two buffers).
  * Debugging aid: with the environment variable FP8Q_DEBUG_INJECT_TIMEOUT=1 set
  * when a GEMM is called, that GEMM waits on a barrier that nothing signals,
  * gives up after 20 ms and takes the timeout path.
