@@ -24,7 +24,7 @@
 //   warps 10-11 idle (they complete the third warpgroup).
 // BN = 256 needs 128 accumulators + 64 staging registers per promotion thread:
 // the kernel is launched with 168 registers per thread (384 x 168 = 64512) and
-// setmaxnreg moves them (128 x 40 + 256 x 232 = 64512). The host refuses to
+// setmaxnreg moves them (128 x 24 + 256 x 240 = 64512). The host refuses to
 // launch unless the compiled count is exactly kLaunchRegs.
 // Scales reach the promotion warps through a per-warp shared-memory ring fed
 // by cp.async three chunks ahead.
@@ -55,8 +55,8 @@ constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kThreads = 384;
 constexpr int kLaunchRegs = 168;
-constexpr int kPromoRegs = 232;
-constexpr int kCtrlRegs = 40;
+constexpr int kPromoRegs = 240;
+constexpr int kCtrlRegs = 24;
 static_assert(kThreads * kLaunchRegs >= 256 * kPromoRegs + 128 * kCtrlRegs,
               "register split exceeds the launch budget");
 constexpr int kScaleSlots = 4;  // per promotion warp
@@ -172,34 +172,41 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
-// a += b * c on two float32 lanes at once (each lane one fused multiply-add,
-// rounded once, as fmaf).
-__device__ __forceinline__ void ffma2(float& a0, float& a1, float b0, float b1, float c0,
-                                      float c1) {
-  asm("{\n\t.reg .b64 ra, rb, rc;\n\t"
-      "mov.b64 ra, {%0, %1};\n\tmov.b64 rb, {%2, %3};\n\tmov.b64 rc, {%4, %5};\n\t"
-      "fma.rn.f32x2 ra, rb, rc, ra;\n\tmov.b64 {%0, %1}, ra;\n\t}"
-      : "+f"(a0), "+f"(a1)
-      : "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+// Pairs of float32 held in one 64-bit register pair (low half = even column),
+// so that the packed f32x2 instructions need no register moves.
+__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
+  uint64_t d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
+  return d;
 }
-// d = a * b on two lanes (each rounded once, as __fmul_rn).
-__device__ __forceinline__ void fmul2(float& d0, float& d1, float a0, float a1, float b0,
-                                      float b1) {
-  asm("{\n\t.reg .b64 rd, ra, rb;\n\t"
-      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
-      "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
-      : "=f"(d0), "=f"(d1)
-      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+__device__ __forceinline__ void unpack2(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+// acc += (p0, p1) * s2, two lanes, each a single-rounding fused multiply-add
+// (as fmaf). p0/p1 come from one TMEM load vector (an aligned register pair).
+__device__ __forceinline__ void ffma2(uint64_t& acc, uint32_t p0, uint32_t p1, uint64_t s2) {
+  asm("{\n\t.reg .b64 rp;\n\tmov.b64 rp, {%1, %2};\n\t"
+      "fma.rn.f32x2 %0, rp, %3, %0;\n\t}"
+      : "+l"(acc)
+      : "r"(p0), "r"(p1), "l"(s2));
+}
+// a * b on two lanes, each rounded once (as __fmul_rn).
+__device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
 }
 
-// Position of a promotion warp's scale prefetch in its (tile, unit) stream,
-// with the tile it last looked up.
+// Position of a promotion warp's scale prefetch in its (tile, unit) stream and
+// the current tile's scale sources for this lane.
 struct ScaleStream {
-  int t;       // tile
-  int u;       // unit (K-block, or 0 without promotion)
-  uint32_t n;  // units issued so far (ring slot = n % kScaleSlots)
-  int cached_t;
-  Tile tl;
+  int t;               // tile
+  int u;               // unit (K-block, or 0 without promotion)
+  uint32_t n;          // units issued so far (ring slot = n % kScaleSlots)
+  int cached_t;        // tile the pointers below belong to
+  const float* sa_src; // &sa[0][m] of this lane's row (valid if sa_ok)
+  const float* sb_src; // &sb[e][0][col0/128], or &sb1[0][col0 + 4*lane]
+  bool sa_ok, sb_ok;
 };
 
 // Copy (cp.async) the scales one promotion warp needs for the next unit of its
@@ -215,26 +222,23 @@ __device__ __forceinline__ void issue_scales(ScaleStream& ss, const Params& p, c
   const uint32_t dst = ring_s + (ss.n % kScaleSlots) * (C::kSlotFloats * 4);
   if (ss.t < total) {
     if (ss.t != ss.cached_t) {
-      ss.tl = tile_at(ss.t, seg, pre, p.E, nt, p.N, p.group_m, BN);
+      const Tile tl = tile_at(ss.t, seg, pre, p.E, nt, p.N, p.group_m, BN);
+      const int64_t m = tl.m0 + q * 32 + lane;
+      const int col0 = tl.n0 + h * C::kWarpCols;
+      ss.sa_ok = m < tl.m_end;
+      ss.sa_src = p.sa + (ss.sa_ok ? m : 0);
+      ss.sb_ok = col0 < p.N;
+      ss.sb_src = sb1 ? p.sb + (ss.sb_ok ? col0 + 4 * lane : 0)
+                      : p.sb + static_cast<int64_t>(tl.e) * KB * NB + (ss.sb_ok ? col0 / 128 : 0);
       ss.cached_t = ss.t;
     }
-    const Tile& tl = ss.tl;
     const int kb = promote ? ss.u : 0;
-    const int64_t m = tl.m0 + q * 32 + lane;
-    const bool rok = m < tl.m_end;
-    cp_async_4(dst + 4u * lane, p.sa + static_cast<int64_t>(kb) * p.M + (rok ? m : 0),
-               rok ? 4u : 0u);
-    const int col0 = tl.n0 + h * C::kWarpCols;
-    const bool cok = col0 < p.N;
+    cp_async_4(dst + 4u * lane, ss.sa_src + static_cast<int64_t>(kb) * p.M, ss.sa_ok ? 4u : 0u);
     if (!sb1) {
-      if (lane == 0) {
-        const float* src =
-            p.sb + (static_cast<int64_t>(tl.e) * KB + kb) * NB + (cok ? col0 / 128 : 0);
-        cp_async_4(dst + 4u * 32, src, cok ? 4u : 0u);
-      }
+      if (lane == 0) cp_async_4(dst + 4u * 32, ss.sb_src + kb * NB, ss.sb_ok ? 4u : 0u);
     } else if (lane < C::kWarpCols / 4) {
-      const float* src = p.sb + static_cast<int64_t>(kb) * p.N + (cok ? col0 + 4 * lane : 0);
-      cp_async_16(dst + 4u * (32 + 4 * lane), src, cok ? 16u : 0u);
+      cp_async_16(dst + 4u * (32 + 4 * lane), ss.sb_src + static_cast<int64_t>(kb) * p.N,
+                  ss.sb_ok ? 16u : 0u);
     }
   }
   cp_async_commit();
@@ -439,9 +443,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
       const Tile tl = tile_at(t, seg, pre, p.E, nt, p.N, p.group_m, BN);
-      float acc[kWarpCols];
+      uint64_t acc[kWarpCols / 2];  // column pairs (2i, 2i+1)
 #pragma unroll
-      for (int j = 0; j < kWarpCols; ++j) acc[j] = 0.0f;
+      for (int j = 0; j < kWarpCols / 2; ++j) acc[j] = 0ull;
 
       for (int u = 0; u < units; ++u) {
         cp_async_wait<kScaleAhead - 1>();
@@ -459,7 +463,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t taddr =
             tmem_base + (static_cast<uint32_t>(q * 32) << 16) + b * BN + h * kWarpCols;
-        const float s_blk = sb1 ? 0.0f : __fmul_rn(sa_v, slot[32]);
+        const uint64_t sa2 = pack2(sa_v, sa_v);
+        uint64_t s_blk2 = 0ull;
+        if (!sb1) {
+          const float s_blk = __fmul_rn(sa_v, slot[32]);
+          s_blk2 = pack2(s_blk, s_blk);
+        }
         constexpr int kRounds = kWarpCols / 64;
 #pragma unroll
         for (int rd = 0; rd < kRounds; ++rd) {
@@ -472,25 +481,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(tempty_bar(b));
           }
-          float* a = acc + rd * 64;
+          uint64_t* a = acc + rd * 32;
           if (!sb1) {
 #pragma unroll
-            for (int j = 0; j < 32; j += 2) {
-              ffma2(a[j], a[j + 1], __uint_as_float(r0[j]), __uint_as_float(r0[j + 1]), s_blk,
-                    s_blk);
-              ffma2(a[32 + j], a[33 + j], __uint_as_float(r1[j]), __uint_as_float(r1[j + 1]),
-                    s_blk, s_blk);
+            for (int j = 0; j < 16; ++j) {
+              ffma2(a[j], r0[2 * j], r0[2 * j + 1], s_blk2);
+              ffma2(a[16 + j], r1[2 * j], r1[2 * j + 1], s_blk2);
             }
           } else {
-            const float* sbv = slot + 32 + rd * 64;
+            const uint64_t* sbv = reinterpret_cast<const uint64_t*>(slot + 32 + rd * 64);
 #pragma unroll
-            for (int j = 0; j < 32; j += 2) {
-              float c0, c1, c2, c3;
-              fmul2(c0, c1, sa_v, sa_v, sbv[j], sbv[j + 1]);
-              fmul2(c2, c3, sa_v, sa_v, sbv[32 + j], sbv[33 + j]);
-              ffma2(a[j], a[j + 1], __uint_as_float(r0[j]), __uint_as_float(r0[j + 1]), c0, c1);
-              ffma2(a[32 + j], a[33 + j], __uint_as_float(r1[j]), __uint_as_float(r1[j + 1]),
-                    c2, c3);
+            for (int j = 0; j < 16; ++j) {
+              ffma2(a[j], r0[2 * j], r0[2 * j + 1], fmul2(sa2, sbv[j]));
+              ffma2(a[16 + j], r1[2 * j], r1[2 * j + 1], fmul2(sa2, sbv[16 + j]));
             }
           }
         }
@@ -504,20 +507,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t m = tl.m0 + q * 32 + lane;
       const int col0 = tl.n0 + h * kWarpCols;
       if (m < tl.m_end && col0 < p.N) {
+        float v[kWarpCols];
+#pragma unroll
+        for (int j = 0; j < kWarpCols / 2; ++j) unpack2(acc[j], v[2 * j], v[2 * j + 1]);
         if (p.flags & kFlagOutBF16) {
           uint4* d = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.D) + m * p.ldd + col0);
 #pragma unroll
           for (int j = 0; j < kWarpCols / 8; ++j) {
-            d[j] = make_uint4(pack_bf16x2(acc[8 * j + 0], acc[8 * j + 1]),
-                              pack_bf16x2(acc[8 * j + 2], acc[8 * j + 3]),
-                              pack_bf16x2(acc[8 * j + 4], acc[8 * j + 5]),
-                              pack_bf16x2(acc[8 * j + 6], acc[8 * j + 7]));
+            d[j] = make_uint4(pack_bf16x2(v[8 * j + 0], v[8 * j + 1]),
+                              pack_bf16x2(v[8 * j + 2], v[8 * j + 3]),
+                              pack_bf16x2(v[8 * j + 4], v[8 * j + 5]),
+                              pack_bf16x2(v[8 * j + 6], v[8 * j + 7]));
           }
         } else {
           float4* d = reinterpret_cast<float4*>(static_cast<float*>(p.D) + m * p.ldd + col0);
 #pragma unroll
           for (int j = 0; j < kWarpCols / 4; ++j)
-            d[j] = make_float4(acc[4 * j], acc[4 * j + 1], acc[4 * j + 2], acc[4 * j + 3]);
+            d[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
         }
       }
     }
