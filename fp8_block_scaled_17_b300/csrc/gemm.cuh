@@ -448,33 +448,41 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < kWarpCols / 2; ++j) acc[j] = 0ull;
 
       for (int u = 0; u < units; ++u) {
+        const uint32_t b = unit % kAccBufs;
+        const bool got = wait_bounded(tfull_bar(b), (unit / kAccBufs) & 1u, abort_flag, p,
+                                      p.wait_limit_ns);
+        tc_fence_after();
+        const uint32_t taddr =
+            tmem_base + (static_cast<uint32_t>(q * 32) << 16) + b * BN + h * kWarpCols;
+        // Start the first TMEM loads right away; the scale ring wait, the scale
+        // reads and the warp vote overlap their latency. (Loading a buffer whose
+        // wait failed reads stale data that is never used.)
+        uint32_t r0[32], r1[32];
+        tmem_ld_32x32b_x32(taddr, r0);
+        tmem_ld_32x32b_x32(taddr + 32, r1);
         cp_async_wait<kScaleAhead - 1>();
         __syncwarp();
         const float* slot = ring + (unit % kScaleSlots) * C::kSlotFloats;
         const float sa_v = slot[lane];
-        const uint32_t b = unit % kAccBufs;
-        // every lane waits; the vote keeps the warp-collective TMEM loads uniform
-        const bool got = wait_bounded(tfull_bar(b), (unit / kAccBufs) & 1u, abort_flag, p,
-                                      p.wait_limit_ns);
-        if (!__all_sync(0xffffffffu, got)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t taddr =
-            tmem_base + (static_cast<uint32_t>(q * 32) << 16) + b * BN + h * kWarpCols;
         const uint64_t sa2 = pack2(sa_v, sa_v);
         uint64_t s_blk2 = 0ull;
         if (!sb1) {
           const float s_blk = __fmul_rn(sa_v, slot[32]);
           s_blk2 = pack2(s_blk, s_blk);
         }
+        // the vote keeps the warp-collective TMEM accesses uniform
+        if (!__all_sync(0xffffffffu, got)) {
+          tmem_ld_wait();
+          ok = false;
+          break;
+        }
         constexpr int kRounds = kWarpCols / 64;
 #pragma unroll
         for (int rd = 0; rd < kRounds; ++rd) {
-          uint32_t r0[32], r1[32];
-          tmem_ld_32x32b_x32(taddr + rd * 64, r0);
-          tmem_ld_32x32b_x32(taddr + rd * 64 + 32, r1);
+          if (rd > 0) {
+            tmem_ld_32x32b_x32(taddr + rd * 64, r0);
+            tmem_ld_32x32b_x32(taddr + rd * 64 + 32, r1);
+          }
           tmem_ld_wait();
           if (rd == kRounds - 1) {  // buffer fully read: hand it back to the MMA issuer
             tc_fence_before();
