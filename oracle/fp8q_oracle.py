@@ -38,9 +38,10 @@ reason, in the design notes of the repository):
     largest finite value 448.
   * Encoding rounds to nearest, ties to the even code, and saturates to +-448.
   * The stored scale is the dequantization scale s = RN32(amax / 448),
-    floored at 2**-126; codes are enc(RN32(x / s)). With the power-of-two
-    option, s = 2**p with p the smallest integer such that amax <= 448 * 2**p
-    (p >= -126).
+    floored at 2**-126. The tile is scaled onto the FP8 range by multiplying
+    with the quantization factor f = RN32(1 / s): codes are enc(RN32(x * f)).
+    With the power-of-two option, s = 2**p with p the smallest integer such
+    that amax <= 448 * 2**p (p >= -126), and f = 2**-p exactly.
   * Promotion interval along K is 128 elements.
   * Re-tiling (1x128 -> 128x1) starts from the cached codes and their scales,
     dequantized exactly as RN32(dec(q) * s).
@@ -134,9 +135,17 @@ def tile_scale(amax, pow2: bool) -> np.ndarray:
     return np.ldexp(np.float32(1.0), p).astype(np.float32)
 
 
+def quant_factor(s) -> np.ndarray:
+    """Quantization factor f = RN32(1 / s) of a tile with dequantization scale s:
+    the input is scaled onto the FP8 range by multiplying with f [OMG,
+    paragraph on scaling the max-abs of the input to the FP8 maximum]."""
+    return (np.float32(1.0) / np.asarray(s, np.float32)).astype(np.float32)
+
+
 def _quantize_with_scale(x: np.ndarray, s: np.ndarray) -> np.ndarray:
-    """codes = enc(RN32(x / s)) (float32 division, correctly rounded)."""
-    return e4m3_encode(np.asarray(x, np.float32) / np.asarray(s, np.float32))
+    """codes = enc(RN32(x * RN32(1 / s))) (float32 operations, each correctly
+    rounded)."""
+    return e4m3_encode(np.asarray(x, np.float32) * quant_factor(s))
 
 
 # ---------------------------------------------------------------------------

@@ -74,12 +74,13 @@ def scale_of(amax: Fraction, pow2: bool) -> Fraction:
 
 
 def quant_tile(xs: list[float], pow2: bool) -> tuple[list[int], Fraction]:
-    """Codes and scale of one tile of float32 values."""
+    """Codes and scale of one tile of float32 values: enc(RN32(x * RN32(1/s)))."""
     amax = max(abs(Fraction(x)) for x in xs)
     s = scale_of(amax, pow2)
+    f = round_to_f32(1 / s)  # quantization factor RN32(1/s)
     codes = []
     for x in xs:
-        q = round_to_f32(Fraction(x) / s)
+        q = round_to_f32(Fraction(x) * f)
         # the sign of a quotient that rounds to zero is the sign of x
         codes.append(encode(math.copysign(float(q), x) if q == 0 else float(q)))
     return codes, s

@@ -138,6 +138,17 @@ def pin_scale_bruteforce(seed=4, n=400):
             assert Fraction(float(g)) == BF.scale_of(Fraction(float(x)), pow2), (x, pow2)
 
 
+def pin_quant_factor():
+    # f = RN32(1/s): exact rational brute force on random scales, and 2^-j for s = 2^j
+    rng = np.random.default_rng(15)
+    s = (rng.uniform(1, 2, 3000) * np.exp2(rng.integers(-126, 120, 3000))).astype(np.float32)
+    got = O.quant_factor(s)
+    for x, g in zip(s, got):
+        assert Fraction(float(g)) == BF.round_to_f32(1 / Fraction(float(x)))
+    j = np.arange(-126, 127)
+    assert (O.quant_factor(np.exp2(j).astype(np.float32)) == np.exp2(-j).astype(np.float32)).all()
+
+
 def _bf16_tensor(shape, seed, std=1.0, outliers=0):
     g = torch.Generator().manual_seed(seed)
     x = torch.randn(shape, generator=g) * std
@@ -314,7 +325,7 @@ def pin_norms_and_error_measure():
 ALL_PINS = [
     pin_decode_all_codes, pin_encode_roundtrip_and_midpoints, pin_encode_bruteforce,
     pin_encode_library_cast, pin_golden_encodings, pin_golden_tile, pin_scale_closed_forms,
-    pin_scale_bruteforce, lambda: pin_quant_act_bruteforce(False),
+    pin_scale_bruteforce, pin_quant_factor, lambda: pin_quant_act_bruteforce(False),
     lambda: pin_quant_act_bruteforce(True), lambda: pin_quant_w_bruteforce(False),
     lambda: pin_quant_w_bruteforce(True), pin_quant_transposed_bruteforce,
     lambda: pin_requant_bruteforce(False), lambda: pin_requant_bruteforce(True),
