@@ -32,7 +32,22 @@ struct DeviceInfo {
   bool gemm256_ok = false;  // BN = 256: its register split matches the compiled count
   int num_sms = 0;
   unsigned* status = nullptr;
+  // resident CTAs per SM of the persistent quantizer kernels
+  int occ_rows = 1, occ_cols_bf16 = 1, occ_cols_codes = 1;
 };
+
+// Dynamic shared memory and occupancy of a persistent quantizer kernel.
+template <typename Kernel>
+bool setup_quant_kernel(Kernel kernel, int smem, int* occ) {
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+      cudaSuccess)
+    return false;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, 256, smem) != cudaSuccess || n < 1)
+    return false;
+  *occ = *occ == 1 || n < *occ ? n : *occ;  // the smallest over the variants
+  return true;
+}
 
 std::mutex g_mutex;
 DeviceInfo g_dev[kMaxDevices];
@@ -68,6 +83,18 @@ fp8q_status device_info(DeviceInfo** out) {
         return FP8Q_ERR_CUDA;
       d.gemm_ok = fa128.maxThreadsPerBlock >= kThreads;
       d.gemm256_ok = fa256.numRegs == kLaunchRegs && fa256.maxThreadsPerBlock >= kThreads;
+      using namespace fp8q;
+      const int rs = kRowSmemBytes, cs0 = col_smem_bytes<0>(), cs1 = col_smem_bytes<1>();
+      d.occ_rows = d.occ_cols_bf16 = d.occ_cols_codes = 1;
+      if (!setup_quant_kernel(quant_rows_1x128_kernel<false>, rs, &d.occ_rows) ||
+          !setup_quant_kernel(quant_rows_1x128_kernel<true>, rs, &d.occ_rows) ||
+          !setup_quant_kernel(quant_cols_kernel<0, false, false>, cs0, &d.occ_cols_bf16) ||
+          !setup_quant_kernel(quant_cols_kernel<0, false, true>, cs0, &d.occ_cols_bf16) ||
+          !setup_quant_kernel(quant_cols_kernel<0, true, false>, cs0, &d.occ_cols_bf16) ||
+          !setup_quant_kernel(quant_cols_kernel<0, true, true>, cs0, &d.occ_cols_bf16) ||
+          !setup_quant_kernel(quant_cols_kernel<1, false, false>, cs1, &d.occ_cols_codes) ||
+          !setup_quant_kernel(quant_cols_kernel<1, false, true>, cs1, &d.occ_cols_codes))
+        return FP8Q_ERR_CUDA;
       void* addr = nullptr;
       if (cudaGetSymbolAddress(&addr, g_device_status) != cudaSuccess) return FP8Q_ERR_CUDA;
       d.status = static_cast<unsigned*>(addr);
@@ -91,6 +118,12 @@ fp8q_status device_info(DeviceInfo** out) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+// Persistent grid: one wave of resident CTAs, never more CTAs than work units.
+unsigned persistent_grid(int64_t units, int num_sms, int occ) {
+  const int64_t g = static_cast<int64_t>(num_sms) * occ;
+  return static_cast<unsigned>(units < g ? units : g);
+}
 
 fp8q_status launch_status() {
   return cudaGetLastError() == cudaSuccess ? FP8Q_OK : FP8Q_ERR_CUDA;
@@ -194,7 +227,7 @@ FP8Q_API fp8q_status fp8q_quant_act_1x128(const void* x, int64_t M, int64_t K, i
   const bool pow2 = flags & FP8Q_POW2_SCALE;
   if (M < 0 || K <= 0 || K % 128) return FP8Q_ERR_SHAPE;
   if (ldq < K || ldx < (transposed ? M : K)) return FP8Q_ERR_SHAPE;
-  if (K / 128 > 65535 || M >= (1ll << 40)) return FP8Q_ERR_SHAPE;
+  if (K / 128 >= (1ll << 31) || M >= (1ll << 40)) return FP8Q_ERR_SHAPE;
   if (M == 0) return FP8Q_OK;
   if (!x || !q || !sa) return FP8Q_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(q) || !aligned4(sa) || (ldx * 2) % 16 || ldq % 16)
@@ -204,19 +237,23 @@ FP8Q_API fp8q_status fp8q_quant_act_1x128(const void* x, int64_t M, int64_t K, i
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const auto* xb = static_cast<const __nv_bfloat16*>(x);
   if (!transposed) {
-    const dim3 grid(static_cast<unsigned>((M + fp8q::kRowQuantRows - 1) / fp8q::kRowQuantRows),
-                    static_cast<unsigned>(K / 128));
+    const int KB = static_cast<int>(K / 128);
+    const int64_t units = ((M + fp8q::kRowUnitRows - 1) / fp8q::kRowUnitRows) * KB;
+    const unsigned grid = persistent_grid(units, dev->num_sms, dev->occ_rows);
+    const int smem = fp8q::kRowSmemBytes;
     if (pow2)
-      fp8q::quant_rows_1x128_kernel<true><<<grid, 256, 0, s>>>(xb, M, ldx, q, ldq, sa);
+      fp8q::quant_rows_1x128_kernel<true><<<grid, 256, smem, s>>>(xb, M, KB, ldx, q, ldq, sa);
     else
-      fp8q::quant_rows_1x128_kernel<false><<<grid, 256, 0, s>>>(xb, M, ldx, q, ldq, sa);
+      fp8q::quant_rows_1x128_kernel<false><<<grid, 256, smem, s>>>(xb, M, KB, ldx, q, ldq, sa);
   } else {
     // stored [K][M]: R = K rows, Cc = M columns, 128x1 column tiles
-    const dim3 grid(static_cast<unsigned>((M + 127) / 128), static_cast<unsigned>(K / 128));
+    const int64_t tiles = ((M + 127) / 128) * (K / 128);
+    const unsigned grid = persistent_grid(tiles, dev->num_sms, dev->occ_cols_bf16);
+    const int smem = fp8q::col_smem_bytes<0>();
     if (pow2)
-      fp8q::quant_cols_kernel<0, false, true><<<grid, 256, 0, s>>>(x, K, M, ldx, nullptr, q, ldq, sa);
+      fp8q::quant_cols_kernel<0, false, true><<<grid, 256, smem, s>>>(x, K, M, ldx, nullptr, q, ldq, sa);
     else
-      fp8q::quant_cols_kernel<0, false, false><<<grid, 256, 0, s>>>(x, K, M, ldx, nullptr, q, ldq, sa);
+      fp8q::quant_cols_kernel<0, false, false><<<grid, 256, smem, s>>>(x, K, M, ldx, nullptr, q, ldq, sa);
   }
   return launch_status();
 }
@@ -225,17 +262,18 @@ FP8Q_API fp8q_status fp8q_quant_w_128x128(const void* w, int64_t K, int64_t N, u
                                           float* sb, unsigned flags, fp8q_stream_t stream) {
   if (flags & ~static_cast<unsigned>(FP8Q_POW2_SCALE)) return FP8Q_ERR_INVALID_ARG;
   if (K <= 0 || N <= 0 || K % 128 || N % 128) return FP8Q_ERR_SHAPE;
-  if (K / 128 > 65535) return FP8Q_ERR_SHAPE;
+  if (K / 128 >= (1ll << 31) || N / 128 >= (1ll << 31)) return FP8Q_ERR_SHAPE;
   if (!w || !q || !sb) return FP8Q_ERR_INVALID_ARG;
   if (!aligned16(w) || !aligned16(q) || !aligned4(sb)) return FP8Q_ERR_ALIGN;
   DeviceInfo* dev = nullptr;
   if (fp8q_status st = device_info(&dev)) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  const dim3 grid(static_cast<unsigned>(N / 128), static_cast<unsigned>(K / 128));
+  const unsigned grid = persistent_grid((N / 128) * (K / 128), dev->num_sms, dev->occ_cols_bf16);
+  const int smem = fp8q::col_smem_bytes<0>();
   if (flags & FP8Q_POW2_SCALE)
-    fp8q::quant_cols_kernel<0, true, true><<<grid, 256, 0, s>>>(w, K, N, N, nullptr, q, K, sb);
+    fp8q::quant_cols_kernel<0, true, true><<<grid, 256, smem, s>>>(w, K, N, N, nullptr, q, K, sb);
   else
-    fp8q::quant_cols_kernel<0, true, false><<<grid, 256, 0, s>>>(w, K, N, N, nullptr, q, K, sb);
+    fp8q::quant_cols_kernel<0, true, false><<<grid, 256, smem, s>>>(w, K, N, N, nullptr, q, K, sb);
   return launch_status();
 }
 
@@ -245,18 +283,19 @@ FP8Q_API fp8q_status fp8q_requant_1x128_to_128x1(const uint8_t* q_in, const floa
                                                  fp8q_stream_t stream) {
   if (flags & ~static_cast<unsigned>(FP8Q_POW2_SCALE)) return FP8Q_ERR_INVALID_ARG;
   if (T <= 0 || C <= 0 || T % 128 || C % 128) return FP8Q_ERR_SHAPE;
-  if (T / 128 > 65535) return FP8Q_ERR_SHAPE;
+  if (T / 128 >= (1ll << 31) || C / 128 >= (1ll << 31)) return FP8Q_ERR_SHAPE;
   if (!q_in || !s_in || !q_out || !s_out) return FP8Q_ERR_INVALID_ARG;
-  if (!aligned16(q_in) || !aligned16(q_out) || !aligned4(s_in) || !aligned4(s_out))
+  if (!aligned16(q_in) || !aligned16(q_out) || !aligned16(s_in) || !aligned4(s_out))
     return FP8Q_ERR_ALIGN;
   DeviceInfo* dev = nullptr;
   if (fp8q_status st = device_info(&dev)) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  const dim3 grid(static_cast<unsigned>(C / 128), static_cast<unsigned>(T / 128));
+  const unsigned grid = persistent_grid((C / 128) * (T / 128), dev->num_sms, dev->occ_cols_codes);
+  const int smem = fp8q::col_smem_bytes<1>();
   if (flags & FP8Q_POW2_SCALE)
-    fp8q::quant_cols_kernel<1, false, true><<<grid, 256, 0, s>>>(q_in, T, C, C, s_in, q_out, T, s_out);
+    fp8q::quant_cols_kernel<1, false, true><<<grid, 256, smem, s>>>(q_in, T, C, C, s_in, q_out, T, s_out);
   else
-    fp8q::quant_cols_kernel<1, false, false><<<grid, 256, 0, s>>>(q_in, T, C, C, s_in, q_out, T, s_out);
+    fp8q::quant_cols_kernel<1, false, false><<<grid, 256, smem, s>>>(q_in, T, C, C, s_in, q_out, T, s_out);
   return launch_status();
 }
 

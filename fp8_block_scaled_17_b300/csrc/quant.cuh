@@ -9,14 +9,15 @@
 // "OMG! The most effective Deepseek Ever!": the max-abs is mapped to the FP8
 // maximum (448 for E4M3).
 //
-// All kernels are HBM-bound streaming kernels: 16-byte vector loads/stores,
-// the amax reduced with warp shuffles (row tiles) or through shared memory
-// (column tiles and blocks), IEEE float32 division for the quotient (a
-// multiplication by 2^-p, which rounds identically, for power-of-2 scales),
-// and cvt.rn.satfinite for the E4M3 encoding.
+// All kernels stream from and to HBM with 16-byte accesses. The input is
+// scaled onto the FP8 range by multiplying with the quantization factor
+// f = RN32(1/s) of its tile (the reciprocal of the stored dequantization scale
+// s; 2^-p exactly for power-of-2 scales): each code is enc(RN32(x * f)).
 #pragma once
 #include <cuda_bf16.h>
 #include <cstdint>
+
+#include "ptx.cuh"
 
 namespace fp8q {
 
@@ -59,268 +60,301 @@ __device__ __forceinline__ float exp2i(int p) {  // 2^p for -126 <= p <= 127
   return __uint_as_float(static_cast<uint32_t>(p + 127) << 23);
 }
 
-// Scale of one tile and the quotient x / s.
+// Scale and quantization factor of one tile.
 template <bool kPow2>
 struct TileScale {
-  float s;    // dequantization scale (what is stored)
-  float inv;  // 2^-p for power-of-2 scales
+  float s;  // dequantization scale (what is stored)
+  float f;  // quantization factor RN32(1/s) (2^-p for power-of-2 scales)
   TileScale() = default;
-  __device__ __forceinline__ TileScale(float s_, float inv_) : s(s_), inv(inv_) {}
   __device__ __forceinline__ explicit TileScale(float amax) {
     if (kPow2) {
       const int p = pow2_exponent(amax);
       s = exp2i(p);
-      inv = exp2i(-p);
+      f = exp2i(-p);
     } else {
       s = fmaxf(__fdiv_rn(amax, kE4M3Max), kMinScale);
-      inv = 0.0f;
+      f = __frcp_rn(s);
     }
-  }
-  __device__ __forceinline__ float quot(float x) const {
-    return kPow2 ? __fmul_rn(x, inv) : __fdiv_rn(x, s);
   }
 };
 
-// -------------------------------------------------------------------------
-// 1x128 row tiles. CTA = 256 threads = 16 half-warps; a half-warp owns one
-// 128-element row tile (16 lanes x 8 bf16) and a CTA covers 64 rows of one
-// K-block, each thread keeping 4 independent 16-byte loads in flight.
-// -------------------------------------------------------------------------
-constexpr int kRowQuantRows = 64;
-
+// Four codes enc(RN32(x_i * f)) of one tile, packed low byte first.
 template <bool kPow2>
-__global__ void __launch_bounds__(256) quant_rows_1x128_kernel(
-    const __nv_bfloat16* __restrict__ x, int64_t M, int64_t ldx, uint8_t* __restrict__ q,
-    int64_t ldq, float* __restrict__ sa) {
-  const int kb = blockIdx.y;
-  const int64_t row0 = static_cast<int64_t>(blockIdx.x) * kRowQuantRows;
-  const int hw = threadIdx.x >> 4;
-  const int l = threadIdx.x & 15;
-  const int64_t col = static_cast<int64_t>(kb) * 128 + l * 8;
-  uint4 v[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int64_t r = row0 + hw + 16 * i;
-    v[i] = make_uint4(0u, 0u, 0u, 0u);
-    if (r < M) v[i] = __ldcs(reinterpret_cast<const uint4*>(x + r * ldx + col));
-  }
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int64_t r = row0 + hw + 16 * i;
-    const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
-    float f[8];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      f[2 * j] = bf16_lo(w[j]);
-      f[2 * j + 1] = bf16_hi(w[j]);
-    }
-    float amax = 0.0f;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(f[j]));
-    // reduce over the 16 lanes of this half-warp
-#pragma unroll
-    for (int o = 8; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    const TileScale<kPow2> ts(amax);
-    uint2 out;
-    out.x = enc4(ts.quot(f[0]), ts.quot(f[1]), ts.quot(f[2]), ts.quot(f[3]));
-    out.y = enc4(ts.quot(f[4]), ts.quot(f[5]), ts.quot(f[6]), ts.quot(f[7]));
-    if (r < M) {
-      *reinterpret_cast<uint2*>(q + r * ldq + col) = out;
-      if (l == 0) sa[static_cast<int64_t>(kb) * M + r] = ts.s;
-    }
-  }
+__device__ __forceinline__ uint32_t quant4(const TileScale<kPow2>& ts, float x0, float x1,
+                                           float x2, float x3) {
+  return enc4(__fmul_rn(x0, ts.f), __fmul_rn(x1, ts.f), __fmul_rn(x2, ts.f),
+              __fmul_rn(x3, ts.f));
 }
 
 // -------------------------------------------------------------------------
-// Column tiles (128x1, one scale per column of a 128-row slab) or 128x128
-// blocks over an input In[R][Cc]; the codes are emitted transposed:
-// Out[c][r] (row stride ldo bytes). One CTA per 128x128 tile, staged in
-// shared memory so that both the reads (along c) and the writes (along r)
-// are contiguous.
-//   kIn == 0: In is bf16 [R][ldin];
+// 1x128 row tiles. Persistent CTAs of 256 threads = 16 half-warps walk over
+// units of 64 rows x one K-block (a half-warp owns one 128-element row tile:
+// 16 lanes x 8 bf16, four rows per thread). Each thread copies its own four
+// 16-byte chunks of the next kRowStages-1 units into a private shared-memory
+// ring with cp.async, so those loads stay in flight without holding
+// registers, and quantizes the oldest unit from the ring.
+// -------------------------------------------------------------------------
+constexpr int kRowUnitRows = 64;
+constexpr int kRowStages = 4;
+constexpr int kRowSmemBytes = kRowStages * kRowUnitRows * 256;  // 64 KB
+
+template <bool kPow2>
+__global__ void __launch_bounds__(256) quant_rows_1x128_kernel(
+    const __nv_bfloat16* __restrict__ x, int64_t M, int KB, int64_t ldx,
+    uint8_t* __restrict__ q, int64_t ldq, float* __restrict__ sa) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  const int hw = threadIdx.x >> 4;
+  const int l = threadIdx.x & 15;
+  const int64_t n_units = ((M + kRowUnitRows - 1) / kRowUnitRows) * KB;
+  const uint32_t ring = smem_u32(smem);
+
+  // unit u -> rows (u / KB) * 64 .., K-block u % KB
+  auto issue = [&](int64_t u, int stage) {
+    if (u < n_units) {
+      const int64_t row0 = (u / KB) * kRowUnitRows;
+      const int kb = static_cast<int>(u % KB);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int rr = hw + 16 * i;
+        const int64_t r = row0 + rr;
+        const bool ok = r < M;
+        const __nv_bfloat16* src = ok ? x + r * ldx + kb * 128 + l * 8 : x;
+        cp_async_16(ring + ((stage * kRowUnitRows + rr) * 16 + l) * 16, src, ok ? 16u : 0u);
+      }
+    }
+    cp_async_commit();
+  };
+
+  const int64_t u0 = blockIdx.x, G = gridDim.x;
+#pragma unroll
+  for (int s = 0; s < kRowStages - 1; ++s) issue(u0 + s * G, s);
+  for (int64_t k = 0;; ++k) {
+    const int64_t u = u0 + k * G;
+    if (u >= n_units) break;
+    issue(u + (kRowStages - 1) * G, static_cast<int>((k + kRowStages - 1) % kRowStages));
+    cp_async_wait<kRowStages - 1>();  // this thread's chunks of unit u have landed
+    const int stage = static_cast<int>(k % kRowStages);
+    const int64_t row0 = (u / KB) * kRowUnitRows;
+    const int kb = static_cast<int>(u % KB);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int rr = hw + 16 * i;
+      const int64_t r = row0 + rr;
+      const uint4 v =
+          reinterpret_cast<const uint4*>(smem)[(stage * kRowUnitRows + rr) * 16 + l];
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      float f[8];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        f[2 * j] = bf16_lo(w[j]);
+        f[2 * j + 1] = bf16_hi(w[j]);
+      }
+      float amax = 0.0f;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(f[j]));
+#pragma unroll
+      for (int o = 8; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+      const TileScale<kPow2> ts(amax);
+      uint2 out;
+      out.x = quant4(ts, f[0], f[1], f[2], f[3]);
+      out.y = quant4(ts, f[4], f[5], f[6], f[7]);
+      if (r < M) {
+        *reinterpret_cast<uint2*>(q + r * ldq + kb * 128 + l * 8) = out;
+        if (l == 0) sa[static_cast<int64_t>(kb) * M + r] = ts.s;
+      }
+    }
+  }
+  cp_async_wait<0>();
+}
+
+// -------------------------------------------------------------------------
+// Column tiles (128x1: one scale per column of a 128-row slab) or 128x128
+// blocks over an input In[R][Cc]; codes are emitted transposed, Out[c][r] with
+// row stride ldo bytes. Persistent CTAs walk over the 128x128 tiles; the next
+// kColStages-1 tiles stream into a shared-memory ring with cp.async while the
+// oldest is quantized. Tiles are staged as 16-byte chunks whose index is
+// XOR-swizzled with the row, so that both the row-wise staging and the
+// column-wise reads are free of bank conflicts; each thread then holds a small
+// block of the tile in registers, the column max-abs is reduced across lanes
+// and every warp store writes whole 128-byte output rows.
+//   kIn == 0: In is bf16 [R][ldin]; a thread holds 8 rows x 8 columns
+//             (rows 8*rg.., rg = lane % 16; columns 8*cg.., cg = tid / 16).
 //   kIn == 1: In is E4M3 codes [R][ldin] with 1x128 row scales
-//             s_in[c/128][r] (R entries per row): x = RN32(dec(q) * s_row).
+//             s_in[c/128][r] (R entries per row), x = RN32(dec(q) * s_row);
+//             staged as 8-byte units (unit index XOR-swizzled with the row)
+//             and held the same way, 8 rows x 8 columns per thread.
 // Scales: per column s_out[rb*Cc + c]; per block s_out[rb*(Cc/128) + cb].
 // R % 128 == 0. Cc may be ragged only for kIn == 0 without kBlock.
 // -------------------------------------------------------------------------
+constexpr int kColStages = 3;
+template <int kIn>
+__host__ __device__ constexpr int col_tile_bytes() { return 128 * (kIn == 0 ? 256 : 128); }
+template <int kIn>
+__host__ __device__ constexpr int col_smem_bytes() {
+  return kColStages * (col_tile_bytes<kIn>() + 512);
+}
+
 template <int kIn, bool kBlock, bool kPow2>
-__global__ void __launch_bounds__(256) quant_cols_kernel(
+__global__ void __launch_bounds__(256, 2) quant_cols_kernel(
     const void* __restrict__ in, int64_t R, int64_t Cc, int64_t ldin,
     const float* __restrict__ s_in, uint8_t* __restrict__ out, int64_t ldo,
     float* __restrict__ s_out) {
-  constexpr int kPadBf16 = 136;  // bf16 per staged row (272 B: conflict-free columns)
-  constexpr int kPadU8 = 144;    // bytes per staged row of codes
-  __shared__ __align__(16) uint8_t tile_raw[kIn == 0 ? 128 * kPadBf16 * 2 : 128 * kPadU8];
-  __shared__ float red[8][128];
-  __shared__ float srow[128];
-  __shared__ float scol[128];
-  __shared__ float sinv[128];
-  __shared__ float bred[4];
+  constexpr int kTile = col_tile_bytes<kIn>();
+  extern __shared__ __align__(16) uint8_t smem[];  // [stage][tile] then [stage][128] row scales
+  __shared__ float red[8];
 
   const int t = threadIdx.x;
-  const int64_t c0 = static_cast<int64_t>(blockIdx.x) * 128;
-  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 128;
+  const int lane = t & 31;
+  const int warp = t >> 5;
+  const int64_t ncb = (Cc + 127) / 128;
+  const int64_t n_tiles = ncb * (R / 128);
+  const uint32_t ring = smem_u32(smem);
+  const uint32_t srow_ring = ring + kColStages * kTile;
 
-  // ---- stage the tile
-  if (kIn == 0) {
-    const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(in);
-    __nv_bfloat16* tile = reinterpret_cast<__nv_bfloat16*>(tile_raw);
-    const int j = t & 15;
-    const bool full = c0 + 128 <= Cc;
+  // tile u -> column block u % ncb, row block u / ncb
+  auto issue = [&](int64_t u, int stage) {
+    if (u < n_tiles) {
+      const int64_t c0 = (u % ncb) * 128, r0 = (u / ncb) * 128;
+      const uint32_t dst = ring + stage * kTile;
+      if (kIn == 0) {
+        const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(in);
+        const int j = t & 15;
+        const int64_t cj = c0 + 8 * j;
+        const int64_t valid = Cc - cj;  // bf16 elements of this chunk inside the matrix
+        const uint32_t bytes = valid >= 8 ? 16u : valid > 0 ? static_cast<uint32_t>(2 * valid) : 0u;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int r = (t >> 4) + 16 * i;
-      const __nv_bfloat16* p = src + (r0 + r) * ldin + c0 + 8 * j;
-      uint4 v;
-      if (full) {
-        v = __ldcs(reinterpret_cast<const uint4*>(p));
-      } else {
-        uint16_t e[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          e[k] = (c0 + 8 * j + k < Cc) ? __bfloat16_as_ushort(p[k]) : static_cast<uint16_t>(0);
+        for (int i = 0; i < 8; ++i) {
+          const int r = (t >> 4) + 16 * i;
+          const __nv_bfloat16* p = bytes ? src + (r0 + r) * ldin + cj : src;
+          cp_async_16(dst + (r * 16 + (j ^ ((r >> 3) & 7))) * 16, p, bytes);
         }
-        v.x = e[0] | (static_cast<uint32_t>(e[1]) << 16);
-        v.y = e[2] | (static_cast<uint32_t>(e[3]) << 16);
-        v.z = e[4] | (static_cast<uint32_t>(e[5]) << 16);
-        v.w = e[6] | (static_cast<uint32_t>(e[7]) << 16);
+      } else {
+        const uint8_t* src = static_cast<const uint8_t*>(in);
+        const int j = t & 15;  // 8-byte unit of the row
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int r = (t >> 4) + 16 * i;
+          cp_async_8(dst + (r * 16 + (j ^ ((r >> 3) & 15))) * 8, src + (r0 + r) * ldin + c0 + 8 * j);
+        }
+        if (t < 32) cp_async_16(srow_ring + stage * 512 + 16 * t, s_in + (c0 / 128) * R + r0 + 4 * t, 16u);
       }
-      *reinterpret_cast<uint4*>(tile + r * kPadBf16 + 8 * j) = v;
     }
-  } else {
-    const uint8_t* src = static_cast<const uint8_t*>(in);
-    const int j = t & 7;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int r = (t >> 3) + 32 * i;
-      const uint4 v = __ldcs(reinterpret_cast<const uint4*>(src + (r0 + r) * ldin + c0 + 16 * j));
-      *reinterpret_cast<uint4*>(tile_raw + r * kPadU8 + 16 * j) = v;
-    }
-    if (t < 128) srow[t] = s_in[(c0 / 128) * R + r0 + t];
-  }
-  __syncthreads();
+    cp_async_commit();
+  };
 
-  // ---- pass 1: column max-abs
-  if (kIn == 0) {
-    const __nv_bfloat16* tile = reinterpret_cast<const __nv_bfloat16*>(tile_raw);
-    const int cp = t & 63, rg = t >> 6;  // column pair, 32-row group
-    float a0 = 0.0f, a1 = 0.0f;
-#pragma unroll 8
-    for (int rr = 0; rr < 32; ++rr) {
-      const uint32_t w =
-          *reinterpret_cast<const uint32_t*>(tile + (rg * 32 + rr) * kPadBf16 + 2 * cp);
-      a0 = fmaxf(a0, fabsf(bf16_lo(w)));
-      a1 = fmaxf(a1, fabsf(bf16_hi(w)));
-    }
-    red[rg][2 * cp] = a0;
-    red[rg][2 * cp + 1] = a1;
-  } else {
-    const int cq = t & 31, rg = t >> 5;  // column quad, 16-row group
-    float a[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll 4
-    for (int rr = 0; rr < 16; ++rr) {
-      const int r = rg * 16 + rr;
-      const uint32_t w = *reinterpret_cast<const uint32_t*>(tile_raw + r * kPadU8 + 4 * cq);
-      const float2 lo = dec2(w & 0xFFFFu), hi = dec2(w >> 16);
-      const float s = srow[r];
-      a[0] = fmaxf(a[0], fabsf(__fmul_rn(lo.x, s)));
-      a[1] = fmaxf(a[1], fabsf(__fmul_rn(lo.y, s)));
-      a[2] = fmaxf(a[2], fabsf(__fmul_rn(hi.x, s)));
-      a[3] = fmaxf(a[3], fabsf(__fmul_rn(hi.y, s)));
-    }
+  const int64_t u0 = blockIdx.x, G = gridDim.x;
 #pragma unroll
-    for (int k = 0; k < 4; ++k) red[rg][4 * cq + k] = a[k];
-  }
-  __syncthreads();
+  for (int s = 0; s < kColStages - 1; ++s) issue(u0 + s * G, s);
+  for (int64_t k = 0;; ++k) {
+    const int64_t u = u0 + k * G;
+    if (u >= n_tiles) break;
+    __syncthreads();  // everyone is done with the buffer the next issue overwrites
+    issue(u + (kColStages - 1) * G, static_cast<int>((k + kColStages - 1) % kColStages));
+    cp_async_wait<kColStages - 1>();
+    __syncthreads();  // tile u has landed, all threads' chunks
+    const int stage = static_cast<int>(k % kColStages);
+    const uint4* tile = reinterpret_cast<const uint4*>(smem + stage * kTile);
+    const int64_t cb = u % ncb, rb = u / ncb;
+    const int64_t c0 = cb * 128, r0 = rb * 128;
 
-  constexpr int kGroups = kIn == 0 ? 4 : 8;
-  if (t < 128) {
-    float a = red[0][t];
+    if (kIn == 0) {
+      const int rg = t & 15, cg = t >> 4;
+      uint32_t w[8][4];  // rows 8*rg + i, columns 8*cg + 2k (low) and 2k+1 (high)
 #pragma unroll
-    for (int g = 1; g < kGroups; ++g) a = fmaxf(a, red[g][t]);
-    if (kBlock) {
+      for (int i = 0; i < 8; ++i) {
+        const uint4 v = tile[(8 * rg + i) * 16 + (cg ^ (rg & 7))];
+        w[i][0] = v.x;
+        w[i][1] = v.y;
+        w[i][2] = v.z;
+        w[i][3] = v.w;
+      }
+      float a[8];
 #pragma unroll
-      for (int o = 16; o >= 1; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
-      if ((t & 31) == 0) bred[t >> 5] = a;
+      for (int kk = 0; kk < 4; ++kk) {
+        float lo = 0.0f, hi = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          lo = fmaxf(lo, fabsf(bf16_lo(w[i][kk])));
+          hi = fmaxf(hi, fabsf(bf16_hi(w[i][kk])));
+        }
+        a[2 * kk] = lo;
+        a[2 * kk + 1] = hi;
+      }
+      // the 16 lanes with this column group hold all 128 rows
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+#pragma unroll
+        for (int o = 1; o <= 8; o <<= 1) a[e] = fmaxf(a[e], __shfl_xor_sync(0xffffffffu, a[e], o));
+      }
+      if (kBlock) {
+        float m = a[0];
+#pragma unroll
+        for (int e = 1; e < 8; ++e) m = fmaxf(m, a[e]);
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));  // the warp's two column groups
+        if (lane == 0) red[warp] = m;
+        __syncthreads();
+        float bm = red[0];
+#pragma unroll
+        for (int w2 = 1; w2 < 8; ++w2) bm = fmaxf(bm, red[w2]);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) a[e] = bm;
+        if (t == 0) s_out[rb * ncb + cb] = TileScale<kPow2>(bm).s;
+      }
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const TileScale<kPow2> ts(a[e]);
+        const int64_t c = c0 + 8 * cg + e;
+        if (!kBlock && rg == 0 && c < Cc) s_out[rb * Cc + c] = ts.s;
+        const int kk = e >> 1;
+        float xv[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) xv[i] = (e & 1) ? bf16_hi(w[i][kk]) : bf16_lo(w[i][kk]);
+        uint2 o;
+        o.x = quant4(ts, xv[0], xv[1], xv[2], xv[3]);
+        o.y = quant4(ts, xv[4], xv[5], xv[6], xv[7]);
+        if (c < Cc) *reinterpret_cast<uint2*>(out + c * ldo + r0 + 8 * rg) = o;
+      }
     } else {
-      const TileScale<kPow2> ts(a);
-      scol[t] = ts.s;
-      sinv[t] = ts.inv;
-      if (c0 + t < Cc) s_out[blockIdx.y * Cc + c0 + t] = ts.s;
-    }
-  }
-  if (kBlock) {
-    __syncthreads();
-    if (t < 128) {
-      const float a = fmaxf(fmaxf(bred[0], bred[1]), fmaxf(bred[2], bred[3]));
-      const TileScale<kPow2> ts(a);
-      scol[t] = ts.s;
-      sinv[t] = ts.inv;
-      if (t == 0) s_out[blockIdx.y * (Cc / 128) + blockIdx.x] = ts.s;
-    }
-  }
-  __syncthreads();
-
-  // ---- pass 2: quantize and store transposed
-  if (kIn == 0) {
-    const __nv_bfloat16* tile = reinterpret_cast<const __nv_bfloat16*>(tile_raw);
-    const int cp = t & 63, rg = t >> 6;
-    const TileScale<kPow2> ts0(scol[2 * cp], sinv[2 * cp]);
-    const TileScale<kPow2> ts1(scol[2 * cp + 1], sinv[2 * cp + 1]);
-    uint32_t o0[8], o1[8];
+      const float* srow = reinterpret_cast<const float*>(smem + kColStages * kTile + stage * 512);
+      const uint2* units = reinterpret_cast<const uint2*>(smem + stage * kTile);
+      const int rg = t & 15, cg = t >> 4;  // rows 8*rg + i, columns 8*cg + e
+      uint2 v[8];
+      float sr[8];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      float x0[4], x1[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const uint32_t w = *reinterpret_cast<const uint32_t*>(
-            tile + (rg * 32 + 4 * k + u) * kPadBf16 + 2 * cp);
-        x0[u] = ts0.quot(bf16_lo(w));
-        x1[u] = ts1.quot(bf16_hi(w));
+      for (int i = 0; i < 8; ++i) {
+        const int r = 8 * rg + i;
+        v[i] = units[r * 16 + (cg ^ rg)];
+        sr[i] = srow[r];
       }
-      o0[k] = enc4(x0[0], x0[1], x0[2], x0[3]);
-      o1[k] = enc4(x1[0], x1[1], x1[2], x1[3]);
-    }
-    const int64_t ca = c0 + 2 * cp;
-    if (ca < Cc) {
-      uint4* d = reinterpret_cast<uint4*>(out + ca * ldo + r0 + rg * 32);
-      d[0] = make_uint4(o0[0], o0[1], o0[2], o0[3]);
-      d[1] = make_uint4(o0[4], o0[5], o0[6], o0[7]);
-    }
-    if (ca + 1 < Cc) {
-      uint4* d = reinterpret_cast<uint4*>(out + (ca + 1) * ldo + r0 + rg * 32);
-      d[0] = make_uint4(o1[0], o1[1], o1[2], o1[3]);
-      d[1] = make_uint4(o1[4], o1[5], o1[6], o1[7]);
-    }
-  } else {
-    const int cq = t & 31, rg = t >> 5;
-    TileScale<kPow2> ts[4];
+      // value in row i, column e: RN32(dec(code) * s_row)
+      auto val = [&](int i, int e) {
+        const uint32_t wd = e < 4 ? v[i].x : v[i].y;
+        const float2 d = dec2((wd >> (8 * (e & 2))) & 0xFFFFu);
+        return __fmul_rn((e & 1) ? d.y : d.x, sr[i]);
+      };
+      float a[8];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) ts[k] = TileScale<kPow2>(scol[4 * cq + k], sinv[4 * cq + k]);
-    uint32_t o[4][4];
+      for (int e = 0; e < 8; ++e) {
+        a[e] = 0.0f;
 #pragma unroll
-    for (int k4 = 0; k4 < 4; ++k4) {  // 4 rows at a time -> one word per column
-      float x[4][4];
+        for (int i = 0; i < 8; ++i) a[e] = fmaxf(a[e], fabsf(val(i, e)));
+        // the 16 lanes with this column group hold all 128 rows
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int r = rg * 16 + 4 * k4 + u;
-        const uint32_t w = *reinterpret_cast<const uint32_t*>(tile_raw + r * kPadU8 + 4 * cq);
-        const float2 lo = dec2(w & 0xFFFFu), hi = dec2(w >> 16);
-        const float s = srow[r];
-        x[0][u] = ts[0].quot(__fmul_rn(lo.x, s));
-        x[1][u] = ts[1].quot(__fmul_rn(lo.y, s));
-        x[2][u] = ts[2].quot(__fmul_rn(hi.x, s));
-        x[3][u] = ts[3].quot(__fmul_rn(hi.y, s));
+        for (int o = 1; o <= 8; o <<= 1) a[e] = fmaxf(a[e], __shfl_xor_sync(0xffffffffu, a[e], o));
       }
 #pragma unroll
-      for (int k = 0; k < 4; ++k) o[k][k4] = enc4(x[k][0], x[k][1], x[k][2], x[k][3]);
-    }
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      *reinterpret_cast<uint4*>(out + (c0 + 4 * cq + k) * ldo + r0 + rg * 16) =
-          make_uint4(o[k][0], o[k][1], o[k][2], o[k][3]);
+      for (int e = 0; e < 8; ++e) {
+        const TileScale<kPow2> ts(a[e]);
+        const int64_t c = c0 + 8 * cg + e;
+        if (rg == 0) s_out[rb * Cc + c] = ts.s;
+        uint2 o;
+        o.x = quant4(ts, val(0, e), val(1, e), val(2, e), val(3, e));
+        o.y = quant4(ts, val(4, e), val(5, e), val(6, e), val(7, e));
+        *reinterpret_cast<uint2*>(out + c * ldo + r0 + 8 * rg) = o;
+      }
     }
   }
+  cp_async_wait<0>();
 }
 
 }  // namespace fp8q

@@ -23,8 +23,10 @@
  *     448), round-to-nearest-even with saturation to +-448. Scales are float32
  *     DEQUANTIZATION scales: value ~= dec(code) * scale. A tile's scale is
  *     s = max(RN32(amax / 448), 2^-126), or with FP8Q_POW2_SCALE the least
- *     power of two 2^p (p >= -126) with amax <= 448 * 2^p; codes are
- *     enc(RN32(x / s)) with IEEE float32 division. Inputs must be finite.
+ *     power of two 2^p (p >= -126) with amax <= 448 * 2^p. The tile is scaled
+ *     onto the FP8 range by its quantization factor f = RN32(1 / s) (2^-p
+ *     exactly for power-of-two scales): codes are enc(RN32(x * f)), each step
+ *     an IEEE float32 operation. Inputs must be finite.
  *   - All pointers are DEVICE pointers owned by the caller. The library
  *     allocates no device memory; it keeps only host-side state (function
  *     attributes, the tensor-map encoder entry point) and one device status
@@ -104,7 +106,7 @@ fp8q_status fp8q_quant_w_128x128(const void* w, int64_t K, int64_t N, uint8_t* q
  * with one scale per 128 tokens of one channel.
  * q_out : uint8 codes [C][T] (transposed: T-major, so Wgrad contracts over
  *         contiguous tokens); s_out float32 [T/128][C].
- * T % 128 == 0 and C % 128 == 0, both > 0; q_in, q_out 16-byte aligned.
+ * T % 128 == 0 and C % 128 == 0, both > 0; q_in, q_out, s_in 16-byte aligned.
  * flags: FP8Q_POW2_SCALE (apply the power-of-two rule to the new tiles).
  */
 fp8q_status fp8q_requant_1x128_to_128x1(const uint8_t* q_in, const float* s_in, int64_t T,
