@@ -48,7 +48,10 @@ METRIC = ("FP8 block-scaled GEMM TFLOP/s (% B300 FP8 peak); "
 # DRAM traffic per launch of the dominant kernel of a workload, from one ncu
 # capture of the same command (dram__bytes_read.sum + dram__bytes_write.sum);
 # an entry is removed whenever that kernel changes.
-TRAFFIC: dict = {}
+TRAFFIC: dict = {
+    # gemm_blockscaled_kernel<256>, dense forward 8192x7168x7168, bf16 out
+    ("dense_fwd", "gemm_blockscaled"): 248249344 + 91746304,
+}
 
 
 # --------------------------------------------------------------------------- setup
@@ -390,6 +393,26 @@ def aggregate(local_seconds: float, local_work: float, reduce_max, reduce_sum):
     return reduce_sum(local_work) / t, t
 
 
+def make_reducers(world: int, device):
+    """max / sum over ranks of a host float, and a barrier (identity at N = 1)."""
+    import torch
+    import torch.distributed as dist
+
+    def reduce(x, op):
+        if world == 1:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=op)
+        return float(t.item())
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    return (lambda x: reduce(x, dist.ReduceOp.MAX), lambda x: reduce(x, dist.ReduceOp.SUM),
+            barrier)
+
+
 def cpu_threads() -> int:
     try:
         from threadpoolctl import threadpool_info
@@ -436,23 +459,7 @@ def run_ours(args):
     device = torch.device("cuda", local)
     legs = set(args.legs.split(","))
 
-    def rmax(x):
-        if world == 1:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
-
-    def rsum(x):
-        if world == 1:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.SUM)
-        return float(t.item())
-
-    def barrier():
-        if world > 1:
-            dist.barrier()
+    rmax, rsum, barrier = make_reducers(world, device)
 
     wl = make_workload(args.workload, device)
     peaks = load_peaks()
