@@ -99,8 +99,8 @@ fp8q_status fp8q_quant_w_128x128(const void* w, int64_t K, int64_t N, uint8_t* q
 
 /*
  * Backward-pass re-tiling of a cached FP8 activation from 1x128 to 128x1
- * tiles [WHY-BE, paragraph "transformed from an 1x128 quantization tile to an
- * 128x1 tile in the backward pass"; paragraph on caching activations in FP8].
+ * tiles [WHY-BE, paragraph on re-tiling activations for the backward pass;
+ * paragraph on caching activations in FP8].
  * q_in  : uint8 codes [T][C] (1x128 tiles along C), s_in float32 [C/128][T].
  * Each value is dequantized as x' = RN32(dec(q) * s_row) and re-quantized
  * with one scale per 128 tokens of one channel.

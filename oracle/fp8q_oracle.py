@@ -13,12 +13,13 @@ Sources (five web pages on DeepSeek-V3's FP8 training recipe; cited by page
 title, or by host name for the two pages that print no title):
 
 [WHY-BE]  why-be.co.kr board post (as_center, wr_id 61844):
-          - paragraph "Delayed quantization ... 1x128 activation tile or
-            128x128 weight block": online max-abs per tile, E4M3 on all
-            tensors, FP8 activation caching, ~2% max relative error at K=4096;
-          - paragraph "these activations can be transformed from an 1x128
-            quantization tile to an 128x1 tile in the backward pass ...
-            scaling factors ... integral power of 2".
+          - paragraph contrasting delayed (history-based) quantization with an
+            online max-abs per 1x128 activation tile and per 128x128 weight
+            block; E4M3 on all tensors, FP8 activation caching, ~2% max
+            relative error at K=4096;
+          - paragraph on re-tiling cached activations from 1x128 to 128x1 for
+            the backward pass, with power-of-two scaling factors for some of
+            them.
 [OMG]     "OMG! The most effective Deepseek Ever!" (thedaegu.com):
           - paragraph on grouping (small groups share exponent bits) and on
             scaling the max-abs of the input to the FP8 maximum;
@@ -28,9 +29,9 @@ title, or by host name for the two pages that print no title):
             Figure 6 (Fprop, Dgrad and Wgrad all in FP8).
 [FOOLED]  "Don't Be Fooled By Deepseek Chatgpt": paragraph on promotion to
           CUDA cores for higher precision, Figure 7 (b).
-[HEARAON] hearaon.co.kr board post (wr_id 810961): paragraph "Higher FP8 GEMM
-          Accumulation Precision in Tensor Cores" (Hopper keeps 14 bits of
-          each aligned mantissa product).
+[HEARAON] hearaon.co.kr board post (wr_id 810961): paragraph on FP8 GEMM
+          accumulation precision in Hopper tensor cores (14 bits of each
+          aligned mantissa product are kept).
 
 Readings taken where the pages are silent (each one is listed, with its
 reason, in the design notes of the repository):
@@ -113,15 +114,14 @@ def tile_scale(amax, pow2: bool) -> np.ndarray:
 
     The max-abs of the tile is mapped onto the largest FP8 value [OMG,
     paragraph on aligning the input's max-abs with the FP8 maximum;
-    WHY-BE, paragraph "we calculate the maximum absolute value online for
-    each 1x128 activation tile or 128x128 weight block ... derive the scaling
-    factor"].
+    WHY-BE, paragraph on the online max-abs per tile or block, from which the
+    scaling factor is derived].
 
     default: s = RN32(amax / 448), floored at 2**-126 so that an all-zero
              tile still has a finite, positive scale.
     pow2:    s = 2**p, p the smallest integer with amax <= 448 * 2**p, floored
-             at -126 [WHY-BE, paragraph "scaling factors for this activation
-             are integral power of 2"]. With amax = f * 2**e, f in [0.5, 1):
+             at -126 [WHY-BE, paragraph on power-of-two scaling factors for
+             some activations]. With amax = f * 2**e, f in [0.5, 1):
              448 = 0.875 * 2**9, so p = e - 9 when f <= 0.875, else e - 8.
     """
     amax = np.asarray(amax, dtype=np.float32)
