@@ -195,3 +195,16 @@ def test_ksweep_full_accuracy(F, K):
         print(f"K={K} {name}: max|C-R|/max|R| = {O.max_relative_error(d[rows], ref):.3e}, "
               f"max|C-R|/(|a_i||b_j|) = {(err / norm).max():.3e}")
     assert_gemm_close(d_p[rows], ref, na, nb, "f32")
+
+
+def test_partial_last_wave(F):
+    """151 tiles of 128 x 256 on a 148-SM grid (a nearly empty last wave):
+    every output against the oracle, and bitwise reproducible."""
+    props = torch.cuda.get_device_properties(0)
+    M, N, K = 128 * (props.multi_processor_count + 3), 256, 1024
+    qa, sa, qb, sb = _quantized_problem(F, M, N, K, seed=77)
+    d1 = F.gemm_blockscaled(qa, sa, qb, sb, out_dtype=torch.float32)
+    d2 = F.gemm_blockscaled(qa, sa, qb, sb, out_dtype=torch.float32)
+    assert F.get_status() == F.OK
+    assert torch.equal(d1, d2)
+    _full_check(d1, qa, sa, qb, sb, "f32")
