@@ -21,13 +21,17 @@
 //   warp 8     TMA producer: A (128 x 128 B) and B (BN x 128 B) tiles into a
 //              shared-memory ring, 128-byte swizzled.
 //   warp 9     TMEM allocator + MMA issuer (one thread).
-//   warps 10-11 idle (they complete the third warpgroup).
+//   warp 10    scale loader: copies (cp.async) the scales of each chunk into a
+//              shared-memory ring: sa of the tile's 128 rows and the B scales
+//              of its columns.
+//   warp 11    idle (it completes the third warpgroup).
 // BN = 256 needs 128 accumulators + 64 staging registers per promotion thread:
 // the kernel is launched with 168 registers per thread (384 x 168 = 64512) and
 // setmaxnreg moves them (128 x 24 + 256 x 240 = 64512). The host refuses to
 // launch unless the compiled count is exactly kLaunchRegs.
-// Scales reach the promotion warps through a per-warp shared-memory ring fed
-// by cp.async three chunks ahead.
+// The promotion warps only read the scale ring (two shared loads per chunk)
+// and release each slot; keeping the global loads off them matters, since
+// their instruction issue is what bounds the kernel.
 //
 // Every wait is bounded in time. A wait that gives up raises a CTA-wide abort
 // flag and the device status word; all roles then stop, the producer waits for
@@ -53,14 +57,14 @@ constexpr int kABytes = BM * BK;  // 16 KB
 constexpr int kPromoWarps = 8;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
+constexpr int kScaleWarp = 10;
 constexpr int kThreads = 384;
 constexpr int kLaunchRegs = 168;
-constexpr int kPromoRegs = 240;
-constexpr int kCtrlRegs = 24;
+constexpr int kPromoRegs = 232;
+constexpr int kCtrlRegs = 40;
 static_assert(kThreads * kLaunchRegs >= 256 * kPromoRegs + 128 * kCtrlRegs,
               "register split exceeds the launch budget");
-constexpr int kScaleSlots = 4;  // per promotion warp
-constexpr int kScaleAhead = 3;  // chunks of scales in flight
+constexpr int kScaleSlots = 8;  // chunks of scales in flight
 constexpr uint32_t kTmemCols = 512;
 constexpr int kMaxExperts = 1024;
 
@@ -74,15 +78,17 @@ struct Cfg {
   static constexpr int kStages = BN == 256 ? 4 : 6;
   static constexpr int kAccBufs = 512 / BN;
   static constexpr int kWarpCols = BN / 2;  // accumulator columns per promotion thread
-  static constexpr int kSlotFloats = 32 + kWarpCols;
+  // scale slot: sa of 128 rows, then B scales (one per 128-column block, or
+  // one per column in 1x128 mode)
+  static constexpr int kSlotFloats = BM + BN;
   static constexpr bool kSplitRegs = BN == 256;
   // shared memory layout (offsets from a 1024-byte aligned base)
   static constexpr uint32_t a_off = 0;
   static constexpr uint32_t b_off = a_off + kStages * kABytes;
   static constexpr uint32_t scale_off = b_off + kStages * kBBytes;
-  static constexpr uint32_t scale_bytes = kPromoWarps * kScaleSlots * kSlotFloats * 4;
+  static constexpr uint32_t scale_bytes = kScaleSlots * kSlotFloats * 4;
   static constexpr uint32_t bar_off = scale_off + scale_bytes;
-  static constexpr uint32_t n_bars = 2 * kStages + 2 * kAccBufs + 2;
+  static constexpr uint32_t n_bars = 2 * kStages + 2 * kAccBufs + 2 + 2 * kScaleSlots;
   static constexpr uint32_t misc_off = bar_off + n_bars * 8;  // tmem base, abort flag
   static constexpr uint32_t table_off = misc_off + 16;        // seg[E+1], prefix[E+1]
   static constexpr uint32_t bytes(int E) { return table_off + 8u * (E + 1) + 1024u; }
@@ -197,58 +203,6 @@ __device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
   return d;
 }
 
-// Position of a promotion warp's scale prefetch in its (tile, unit) stream and
-// the current tile's scale sources for this lane.
-struct ScaleStream {
-  int t;               // tile
-  int u;               // unit (K-block, or 0 without promotion)
-  uint32_t n;          // units issued so far (ring slot = n % kScaleSlots)
-  int cached_t;        // tile the pointers below belong to
-  const float* sa_src; // &sa[0][m] of this lane's row (valid if sa_ok)
-  const float* sb_src; // &sb[e][0][col0/128], or &sb1[0][col0 + 4*lane]
-  bool sa_ok, sb_ok;
-};
-
-// Copy (cp.async) the scales one promotion warp needs for the next unit of its
-// stream into its ring slot: sa of its 32 rows, and either the one 128x128
-// B-block scale of its columns or their per-column B scales. One commit group
-// per unit (empty past the last tile, so that group counting stays uniform).
-template <int BN>
-__device__ __forceinline__ void issue_scales(ScaleStream& ss, const Params& p, const int* seg,
-                                             const int* pre, int nt, int KB, int NB, int units,
-                                             int total, bool promote, bool sb1, int q, int h,
-                                             int lane, uint32_t ring_s) {
-  using C = Cfg<BN>;
-  const uint32_t dst = ring_s + (ss.n % kScaleSlots) * (C::kSlotFloats * 4);
-  if (ss.t < total) {
-    if (ss.t != ss.cached_t) {
-      const Tile tl = tile_at(ss.t, seg, pre, p.E, nt, p.N, p.group_m, BN);
-      const int64_t m = tl.m0 + q * 32 + lane;
-      const int col0 = tl.n0 + h * C::kWarpCols;
-      ss.sa_ok = m < tl.m_end;
-      ss.sa_src = p.sa + (ss.sa_ok ? m : 0);
-      ss.sb_ok = col0 < p.N;
-      ss.sb_src = sb1 ? p.sb + (ss.sb_ok ? col0 + 4 * lane : 0)
-                      : p.sb + static_cast<int64_t>(tl.e) * KB * NB + (ss.sb_ok ? col0 / 128 : 0);
-      ss.cached_t = ss.t;
-    }
-    const int kb = promote ? ss.u : 0;
-    cp_async_4(dst + 4u * lane, ss.sa_src + static_cast<int64_t>(kb) * p.M, ss.sa_ok ? 4u : 0u);
-    if (!sb1) {
-      if (lane == 0) cp_async_4(dst + 4u * 32, ss.sb_src + kb * NB, ss.sb_ok ? 4u : 0u);
-    } else if (lane < C::kWarpCols / 4) {
-      cp_async_16(dst + 4u * (32 + 4 * lane), ss.sb_src + static_cast<int64_t>(kb) * p.N,
-                  ss.sb_ok ? 16u : 0u);
-    }
-  }
-  cp_async_commit();
-  ++ss.n;
-  if (++ss.u == units) {
-    ss.u = 0;
-    ss.t += gridDim.x;
-  }
-}
-
 template <int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_blockscaled_kernel(const __grid_constant__ CUtensorMap tmA,
@@ -272,6 +226,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto tempty_bar = [&](uint32_t b) { return bar0 + 8u * (2 * kStages + kAccBufs + b); };
   const uint32_t drain_bar = bar0 + 8u * (2 * kStages + 2 * kAccBufs);
   const uint32_t never_bar = drain_bar + 8u;
+  auto sfull_bar = [&](uint32_t i) { return never_bar + 8u * (1 + i); };
+  auto sempty_bar = [&](uint32_t i) { return never_bar + 8u * (1 + kScaleSlots + i); };
   uint32_t* const misc = reinterpret_cast<uint32_t*>(base_ptr + C::misc_off);
   volatile uint32_t* const abort_flag = misc + 1;
   int* const seg = reinterpret_cast<int*>(base_ptr + C::table_off);
@@ -300,6 +256,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(drain_bar, 1);
     mbar_init(never_bar, 1);
+    for (uint32_t i = 0; i < kScaleSlots; ++i) {
+      mbar_init(sfull_bar(i), 32);  // one cp.async arrival per loader lane
+      mbar_init(sempty_bar(i), kPromoWarps);
+    }
     misc[1] = 0u;
     fence_mbar_init();
   }
@@ -332,6 +292,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = misc[0];
   const int total = pre[p.E];
+  const bool sb1 = (p.flags & kFlagScaleB1x128) != 0;
+  const int NB = p.N / 128;
+  const int units = promote ? KB : 1;  // scale units (chunks) per tile
 
   if (warp >= kPromoWarps) {
     if constexpr (C::kSplitRegs) setmaxnreg_dec<kCtrlRegs>();
@@ -417,27 +380,68 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       __syncwarp();
+    } else if (warp == kScaleWarp) {
+      // ------------------------------------------------------- scale loader
+      // Slot n % kScaleSlots holds the scales of the n-th unit of this CTA's
+      // stream: sa[kb][m0 .. m0+127] (0 past the tile's rows), then either the
+      // B-block scales of the tile's BN/128 column blocks or, in 1x128 mode,
+      // the BN column scales sb[kb][n0 ..]. Each lane signals the slot's full
+      // barrier when its own copies have landed.
+      const uint32_t ring = base + C::scale_off;
+      uint32_t n = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        const Tile tl = tile_at(t, seg, pre, p.E, nt, p.N, p.group_m, BN);
+        // rows of this lane: m0 + lane + 32 i, valid while below m_end
+        const int64_t left = tl.m_end - tl.m0;
+        const int rows = left < BM ? static_cast<int>(left) : BM;
+        const int cols = p.N - tl.n0;  // columns of B in this tile (BN or fewer)
+        const float* sa_src = p.sa + tl.m0 + lane;
+        // B scales of this lane (block mode: lanes < BN/128; 1x128 mode: 4 columns x BN/128)
+        const float* sb_src = sb1 ? p.sb + tl.n0 + 4 * lane
+                                  : p.sb + static_cast<int64_t>(tl.e) * KB * NB + tl.n0 / 128 + lane;
+        const int64_t sa_step = promote ? p.M : 0;
+        const int64_t sb_step = promote ? (sb1 ? p.N : NB) : 0;
+        for (int u = 0; u < units; ++u, ++n) {
+          const uint32_t slot = n % kScaleSlots;
+          if (!wait_bounded(sempty_bar(slot), ((n / kScaleSlots) & 1u) ^ 1u, abort_flag, p,
+                            p.wait_limit_ns)) {
+            ok = false;
+            break;
+          }
+          const uint32_t dst = ring + slot * (C::kSlotFloats * 4) + 4u * lane;
+#pragma unroll
+          for (int i = 0; i < BM / 32; ++i) {
+            const bool in = 32 * i + lane < rows;
+            cp_async_4(dst + 128u * i, in ? sa_src + 32 * i : p.sa, in ? 4u : 0u);
+          }
+          if (!sb1) {
+            if (lane < BN / 128) {
+              const bool in = 128 * lane < cols;
+              cp_async_4(dst + 4u * BM, in ? sb_src : p.sb, in ? 4u : 0u);
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < BN / 128; ++i) {
+              const bool in = 128 * i + 4 * lane < cols;
+              cp_async_16(dst + 4u * BM + 12u * lane + 512u * i, in ? sb_src + 128 * i : p.sb,
+                          in ? 16u : 0u);
+            }
+          }
+          cp_async_mbar_arrive_noinc(sfull_bar(slot));
+          sa_src += sa_step;
+          sb_src += sb_step;
+        }
+      }
+      cp_async_wait<0>();  // copies in flight land before the CTA exits
+      __syncwarp();
     }
   } else {
     if constexpr (C::kSplitRegs) setmaxnreg_inc<kPromoRegs>();
     // --------------------------------------------------- promotion + epilogue
     const int q = warp & 3;   // TMEM lane quarter -> rows 32q .. 32q+31
     const int h = warp >> 2;  // column half -> columns h*BN/2 ..
-    const bool sb1 = (p.flags & kFlagScaleB1x128) != 0;
-    const int NB = (p.N + 127) / 128;
-    const int units = promote ? KB : 1;
-    const float* const ring = reinterpret_cast<const float*>(base_ptr + C::scale_off) +
-                              warp * kScaleSlots * C::kSlotFloats;
-    const uint32_t ring_s = base + C::scale_off + warp * kScaleSlots * C::kSlotFloats * 4;
-
-    ScaleStream ss;
-    ss.t = blockIdx.x;
-    ss.u = 0;
-    ss.n = 0u;
-    ss.cached_t = -1;
-    for (int i = 0; i < kScaleAhead; ++i)
-      issue_scales<BN>(ss, p, seg, pre, nt, KB, NB, units, total, promote, sb1, q, h, lane,
-                       ring_s);
+    const float* const ring = reinterpret_cast<const float*>(base_ptr + C::scale_off);
 
     uint32_t unit = 0;
     bool ok = true;
@@ -449,26 +453,29 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       for (int u = 0; u < units; ++u) {
         const uint32_t b = unit % kAccBufs;
-        const bool got = wait_bounded(tfull_bar(b), (unit / kAccBufs) & 1u, abort_flag, p,
-                                      p.wait_limit_ns);
+        bool got = wait_bounded(tfull_bar(b), (unit / kAccBufs) & 1u, abort_flag, p,
+                                p.wait_limit_ns);
         tc_fence_after();
         const uint32_t taddr =
             tmem_base + (static_cast<uint32_t>(q * 32) << 16) + b * BN + h * kWarpCols;
-        // Start the first TMEM loads right away; the scale ring wait, the scale
+        // Start the first TMEM loads right away; the scale slot wait, the scale
         // reads and the warp vote overlap their latency. (Loading a buffer whose
         // wait failed reads stale data that is never used.)
         uint32_t r0[32], r1[32];
         tmem_ld_32x32b_x32(taddr, r0);
         tmem_ld_32x32b_x32(taddr + 32, r1);
-        cp_async_wait<kScaleAhead - 1>();
-        __syncwarp();
-        const float* slot = ring + (unit % kScaleSlots) * C::kSlotFloats;
-        const float sa_v = slot[lane];
+        const uint32_t sslot = unit % kScaleSlots;
+        if (got) got = wait_bounded(sfull_bar(sslot), (unit / kScaleSlots) & 1u, abort_flag, p,
+                                    p.wait_limit_ns);
+        const float* slot = ring + sslot * C::kSlotFloats;
+        const float sa_v = slot[q * 32 + lane];
         const uint64_t sa2 = pack2(sa_v, sa_v);
         uint64_t s_blk2 = 0ull;
         if (!sb1) {
-          const float s_blk = __fmul_rn(sa_v, slot[32]);
+          const float s_blk = __fmul_rn(sa_v, slot[BM + (h * kWarpCols) / 128]);
           s_blk2 = pack2(s_blk, s_blk);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(sempty_bar(sslot));  // slot read: release it
         }
         // the vote keeps the warp-collective TMEM accesses uniform
         if (!__all_sync(0xffffffffu, got)) {
@@ -497,7 +504,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               ffma2(a[16 + j], r1[2 * j], r1[2 * j + 1], s_blk2);
             }
           } else {
-            const uint64_t* sbv = reinterpret_cast<const uint64_t*>(slot + 32 + rd * 64);
+            const uint64_t* sbv =
+                reinterpret_cast<const uint64_t*>(slot + BM + h * kWarpCols + rd * 64);
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
               ffma2(a[j], r0[2 * j], r0[2 * j + 1], fmul2(sa2, sbv[j]));
@@ -505,9 +513,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
+        if (sb1) {  // column scales read: release the slot
+          __syncwarp();
+          if (lane == 0) mbar_arrive(sempty_bar(sslot));
+        }
         ++unit;
-        issue_scales<BN>(ss, p, seg, pre, nt, KB, NB, units, total, promote, sb1, q, h, lane,
-                         ring_s);
       }
       if (!ok) break;
 
@@ -535,7 +545,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-    cp_async_wait<0>();
   }
 
   // ---------------------------------------------------------------- teardown
