@@ -64,7 +64,11 @@ constexpr int kPromoRegs = 232;
 constexpr int kCtrlRegs = 40;
 static_assert(kThreads * kLaunchRegs >= 256 * kPromoRegs + 128 * kCtrlRegs,
               "register split exceeds the launch budget");
-constexpr int kScaleSlots = 8;  // chunks of scales in flight
+// Scale ring: slots of several consecutive units (chunks), so that the
+// promotion warps wait for a slot and release it once per group of units;
+// mbarrier operations cost them about as much as a round of FMAs.
+constexpr int kRingFloats = 6144;
+constexpr int kMaxScaleSlots = 8;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kMaxExperts = 1024;
 
@@ -78,17 +82,18 @@ struct Cfg {
   static constexpr int kStages = BN == 256 ? 4 : 6;
   static constexpr int kAccBufs = 512 / BN;
   static constexpr int kWarpCols = BN / 2;  // accumulator columns per promotion thread
-  // scale slot: sa of 128 rows, then B scales (one per 128-column block, or
-  // one per column in 1x128 mode)
-  static constexpr int kSlotFloats = BM + BN;
+  // one unit in the scale ring: sa of 128 rows, then the B scales (one per
+  // 128-column block, or one per column in 1x128 mode)
+  static constexpr int kUnitFloatsBlock = BM + 4;
+  static constexpr int kUnitFloats1x128 = BM + BN;
   static constexpr bool kSplitRegs = BN == 256;
   // shared memory layout (offsets from a 1024-byte aligned base)
   static constexpr uint32_t a_off = 0;
   static constexpr uint32_t b_off = a_off + kStages * kABytes;
   static constexpr uint32_t scale_off = b_off + kStages * kBBytes;
-  static constexpr uint32_t scale_bytes = kScaleSlots * kSlotFloats * 4;
+  static constexpr uint32_t scale_bytes = kRingFloats * 4;
   static constexpr uint32_t bar_off = scale_off + scale_bytes;
-  static constexpr uint32_t n_bars = 2 * kStages + 2 * kAccBufs + 2 + 2 * kScaleSlots;
+  static constexpr uint32_t n_bars = 2 * kStages + 2 * kAccBufs + 2 + 2 * kMaxScaleSlots;
   static constexpr uint32_t misc_off = bar_off + n_bars * 8;  // tmem base, abort flag
   static constexpr uint32_t table_off = misc_off + 16;        // seg[E+1], prefix[E+1]
   static constexpr uint32_t bytes(int E) { return table_off + 8u * (E + 1) + 1024u; }
@@ -227,7 +232,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t drain_bar = bar0 + 8u * (2 * kStages + 2 * kAccBufs);
   const uint32_t never_bar = drain_bar + 8u;
   auto sfull_bar = [&](uint32_t i) { return never_bar + 8u * (1 + i); };
-  auto sempty_bar = [&](uint32_t i) { return never_bar + 8u * (1 + kScaleSlots + i); };
+  auto sempty_bar = [&](uint32_t i) { return never_bar + 8u * (1 + kMaxScaleSlots + i); };
   uint32_t* const misc = reinterpret_cast<uint32_t*>(base_ptr + C::misc_off);
   volatile uint32_t* const abort_flag = misc + 1;
   int* const seg = reinterpret_cast<int*>(base_ptr + C::table_off);
@@ -256,7 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(drain_bar, 1);
     mbar_init(never_bar, 1);
-    for (uint32_t i = 0; i < kScaleSlots; ++i) {
+    for (uint32_t i = 0; i < kMaxScaleSlots; ++i) {
       mbar_init(sfull_bar(i), 32);  // one cp.async arrival per loader lane
       mbar_init(sempty_bar(i), kPromoWarps);
     }
@@ -295,6 +300,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool sb1 = (p.flags & kFlagScaleB1x128) != 0;
   const int NB = p.N / 128;
   const int units = promote ? KB : 1;  // scale units (chunks) per tile
+  // scale ring geometry: units of ustride floats, group_u units per slot
+  const int ustride = sb1 ? C::kUnitFloats1x128 : C::kUnitFloatsBlock;
+  const uint32_t group_u = sb1 ? 4u : 8u;
+  const uint32_t nslots = min(static_cast<uint32_t>(kMaxScaleSlots),
+                              static_cast<uint32_t>(kRingFloats) / (group_u * ustride));
 
   if (warp >= kPromoWarps) {
     if constexpr (C::kSplitRegs) setmaxnreg_dec<kCtrlRegs>();
@@ -350,12 +360,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ok = false;
                 break;
               }
-              tc_fence_after();
             }
             if (!wait_bounded(full_bar(stage), phase, abort_flag, p, p.wait_limit_ns)) {
               ok = false;
               break;
             }
+            // one fence orders these MMAs after both waits: the promotion warps'
+            // TMEM reads of buffer b and the TMA writes of this stage (a fence
+            // per wait costs the tensor pipe measurable time per chunk)
             tc_fence_after();
             const uint64_t adesc = sw128_kmajor_desc(base + C::a_off + stage * kABytes);
             const uint64_t bdesc = sw128_kmajor_desc(base + C::b_off + stage * C::kBBytes);
@@ -382,13 +394,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
     } else if (warp == kScaleWarp) {
       // ------------------------------------------------------- scale loader
-      // Slot n % kScaleSlots holds the scales of the n-th unit of this CTA's
-      // stream: sa[kb][m0 .. m0+127] (0 past the tile's rows), then either the
-      // B-block scales of the tile's BN/128 column blocks or, in 1x128 mode,
-      // the BN column scales sb[kb][n0 ..]. Each lane signals the slot's full
-      // barrier when its own copies have landed.
+      // Unit n of this CTA's stream (tile-major, then K-block) goes to slot
+      // (n / group_u) % nslots, position n % group_u: sa[kb][m0 .. m0+127] (0
+      // past the tile's rows), then either the B-block scales of the tile's
+      // BN/128 column blocks or, in 1x128 mode, the BN column scales
+      // sb[kb][n0 ..]. Once a slot's units are issued, each lane signals the
+      // slot's full barrier for when its own copies have landed.
       const uint32_t ring = base + C::scale_off;
-      uint32_t n = 0;
+      uint32_t sub = 0, slot = 0, sphase = 0;  // position of the next unit in the ring
       bool ok = true;
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
         const Tile tl = tile_at(t, seg, pre, p.E, nt, p.N, p.group_m, BN);
@@ -402,14 +415,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                                   : p.sb + static_cast<int64_t>(tl.e) * KB * NB + tl.n0 / 128 + lane;
         const int64_t sa_step = promote ? p.M : 0;
         const int64_t sb_step = promote ? (sb1 ? p.N : NB) : 0;
-        for (int u = 0; u < units; ++u, ++n) {
-          const uint32_t slot = n % kScaleSlots;
-          if (!wait_bounded(sempty_bar(slot), ((n / kScaleSlots) & 1u) ^ 1u, abort_flag, p,
-                            p.wait_limit_ns)) {
+        for (int u = 0; u < units; ++u) {
+          if (sub == 0 &&
+              !wait_bounded(sempty_bar(slot), sphase ^ 1u, abort_flag, p, p.wait_limit_ns)) {
             ok = false;
             break;
           }
-          const uint32_t dst = ring + slot * (C::kSlotFloats * 4) + 4u * lane;
+          const uint32_t dst = ring + 4u * ((slot * group_u + sub) * ustride + lane);
 #pragma unroll
           for (int i = 0; i < BM / 32; ++i) {
             const bool in = 32 * i + lane < rows;
@@ -428,11 +440,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                           in ? 16u : 0u);
             }
           }
-          cp_async_mbar_arrive_noinc(sfull_bar(slot));
           sa_src += sa_step;
           sb_src += sb_step;
+          if (++sub == group_u) {
+            cp_async_mbar_arrive_noinc(sfull_bar(slot));
+            sub = 0;
+            if (++slot == nslots) { slot = 0; sphase ^= 1u; }
+          }
         }
       }
+      if (ok && sub != 0) cp_async_mbar_arrive_noinc(sfull_bar(slot));  // last, partly filled slot
       cp_async_wait<0>();  // copies in flight land before the CTA exits
       __syncwarp();
     }
@@ -444,6 +461,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float* const ring = reinterpret_cast<const float*>(base_ptr + C::scale_off);
 
     uint32_t unit = 0;
+    // scale ring position: unit ssub of slot sslot (unit sunit of the ring), phase sphase
+    uint32_t ssub = 0, sslot = 0, sunit = 0, sphase = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
       const Tile tl = tile_at(t, seg, pre, p.E, nt, p.N, p.group_m, BN);
@@ -464,18 +483,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t r0[32], r1[32];
         tmem_ld_32x32b_x32(taddr, r0);
         tmem_ld_32x32b_x32(taddr + 32, r1);
-        const uint32_t sslot = unit % kScaleSlots;
-        if (got) got = wait_bounded(sfull_bar(sslot), (unit / kScaleSlots) & 1u, abort_flag, p,
-                                    p.wait_limit_ns);
-        const float* slot = ring + sslot * C::kSlotFloats;
+        if (got && ssub == 0)
+          got = wait_bounded(sfull_bar(sslot), sphase, abort_flag, p, p.wait_limit_ns);
+        const bool release = ssub == group_u - 1;
+        const float* slot = ring + sunit * ustride;
         const float sa_v = slot[q * 32 + lane];
         const uint64_t sa2 = pack2(sa_v, sa_v);
         uint64_t s_blk2 = 0ull;
         if (!sb1) {
           const float s_blk = __fmul_rn(sa_v, slot[BM + (h * kWarpCols) / 128]);
           s_blk2 = pack2(s_blk, s_blk);
-          __syncwarp();
-          if (lane == 0) mbar_arrive(sempty_bar(sslot));  // slot read: release it
+          if (release) {  // the slot's last unit read: release it
+            __syncwarp();
+            if (lane == 0) mbar_arrive(sempty_bar(sslot));
+          }
         }
         // the vote keeps the warp-collective TMEM accesses uniform
         if (!__all_sync(0xffffffffu, got)) {
@@ -513,11 +534,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        if (sb1) {  // column scales read: release the slot
+        if (sb1 && release) {  // column scales read: release the slot
           __syncwarp();
           if (lane == 0) mbar_arrive(sempty_bar(sslot));
         }
         ++unit;
+        ++sunit;
+        if (++ssub == group_u) {
+          ssub = 0;
+          if (++sslot == nslots) { sslot = 0; sunit = 0; sphase ^= 1u; }
+        }
       }
       if (!ok) break;
 
