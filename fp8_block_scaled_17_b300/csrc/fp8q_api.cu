@@ -197,7 +197,9 @@ fp8q_status gemm_common(const uint8_t* A, const float* sa, const int32_t* m_offs
   p.E = E;
   p.flags = ((flags & FP8Q_NO_PROMOTION) ? 0 : kFlagPromote) |
             ((flags & FP8Q_OUT_BF16) ? kFlagOutBF16 : 0) |
-            ((flags & FP8Q_SCALE_B_1x128) ? kFlagScaleB1x128 : 0);
+            ((flags & FP8Q_SCALE_B_1x128) ? kFlagScaleB1x128 : 0) |
+            ((reinterpret_cast<uintptr_t>(D) % 32 == 0 && (ldd * out_bytes) % 32 == 0) ? kFlagStore32
+                                                                                   : 0);
   p.group_m = 16;
   p.tx_bytes = (box_a_rows + box_b_rows) * BK;
   p.inject_timeout = env_flag("FP8Q_DEBUG_INJECT_TIMEOUT") ? 1 : 0;

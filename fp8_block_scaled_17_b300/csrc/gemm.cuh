@@ -27,7 +27,7 @@
 //   warp 11    idle (it completes the third warpgroup).
 // BN = 256 needs 128 accumulators + 64 staging registers per promotion thread:
 // the kernel is launched with 168 registers per thread (384 x 168 = 64512) and
-// setmaxnreg moves them (128 x 24 + 256 x 240 = 64512). The host refuses to
+// setmaxnreg moves them (128 x 40 + 256 x 232 = 64512). The host refuses to
 // launch unless the compiled count is exactly kLaunchRegs.
 // The promotion warps only read the scale ring (two shared loads per chunk)
 // and release each slot; keeping the global loads off them matters, since
@@ -75,6 +75,7 @@ constexpr int kMaxExperts = 1024;
 constexpr int kFlagPromote = 1;
 constexpr int kFlagOutBF16 = 2;
 constexpr int kFlagScaleB1x128 = 4;
+constexpr int kFlagStore32 = 8;  // D and its row pitch are 32-byte aligned
 
 template <int BN>
 struct Cfg {
@@ -554,20 +555,44 @@ __global__ void __launch_bounds__(kThreads, 1)
         float v[kWarpCols];
 #pragma unroll
         for (int j = 0; j < kWarpCols / 2; ++j) unpack2(acc[j], v[2 * j], v[2 * j + 1]);
+        // Each thread writes a row segment; 32-byte stores halve the number of
+        // memory requests of this row-per-thread layout when D allows them.
         if (p.flags & kFlagOutBF16) {
-          uint4* d = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.D) + m * p.ldd + col0);
+          __nv_bfloat16* d = static_cast<__nv_bfloat16*>(p.D) + m * p.ldd + col0;
+          if (p.flags & kFlagStore32) {
 #pragma unroll
-          for (int j = 0; j < kWarpCols / 8; ++j) {
-            d[j] = make_uint4(pack_bf16x2(v[8 * j + 0], v[8 * j + 1]),
-                              pack_bf16x2(v[8 * j + 2], v[8 * j + 3]),
-                              pack_bf16x2(v[8 * j + 4], v[8 * j + 5]),
-                              pack_bf16x2(v[8 * j + 6], v[8 * j + 7]));
+            for (int j = 0; j < kWarpCols / 16; ++j) {
+              const float* w = v + 16 * j;
+              st_global_v8(d + 16 * j, pack_bf16x2(w[0], w[1]), pack_bf16x2(w[2], w[3]),
+                           pack_bf16x2(w[4], w[5]), pack_bf16x2(w[6], w[7]),
+                           pack_bf16x2(w[8], w[9]), pack_bf16x2(w[10], w[11]),
+                           pack_bf16x2(w[12], w[13]), pack_bf16x2(w[14], w[15]));
+            }
+          } else {
+            uint4* d4 = reinterpret_cast<uint4*>(d);
+#pragma unroll
+            for (int j = 0; j < kWarpCols / 8; ++j) {
+              const float* w = v + 8 * j;
+              d4[j] = make_uint4(pack_bf16x2(w[0], w[1]), pack_bf16x2(w[2], w[3]),
+                                 pack_bf16x2(w[4], w[5]), pack_bf16x2(w[6], w[7]));
+            }
           }
         } else {
-          float4* d = reinterpret_cast<float4*>(static_cast<float*>(p.D) + m * p.ldd + col0);
+          float* d = static_cast<float*>(p.D) + m * p.ldd + col0;
+          if (p.flags & kFlagStore32) {
 #pragma unroll
-          for (int j = 0; j < kWarpCols / 4; ++j)
-            d[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+            for (int j = 0; j < kWarpCols / 8; ++j) {
+              const float* w = v + 8 * j;
+              st_global_v8(d + 8 * j, __float_as_uint(w[0]), __float_as_uint(w[1]),
+                           __float_as_uint(w[2]), __float_as_uint(w[3]), __float_as_uint(w[4]),
+                           __float_as_uint(w[5]), __float_as_uint(w[6]), __float_as_uint(w[7]));
+            }
+          } else {
+            float4* d4 = reinterpret_cast<float4*>(d);
+#pragma unroll
+            for (int j = 0; j < kWarpCols / 4; ++j)
+              d4[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+          }
         }
       }
     }

@@ -62,6 +62,24 @@ def test_strided_output(F):
     assert (big[:, :64] == 7).all() and (big[:, 320:] == 7).all()
 
 
+@pytest.mark.parametrize("out", ["bf16", "f32"])
+def test_output_16b_aligned_only(F, out):
+    """D whose base and row pitch are 16- but not 32-byte aligned takes the 16-byte
+    store path; it must give the same bits as a 32-byte aligned D, and leave the
+    elements around it untouched."""
+    M, N, K = 160, 256, 384
+    qa, sa, qb, sb = _quantized_problem(F, M, N, K, seed=91)
+    dt = torch.bfloat16 if out == "bf16" else torch.float32
+    pad = 16 // (2 if out == "bf16" else 4)  # 16 bytes of elements
+    ref = F.gemm_blockscaled(qa, sa, qb, sb, out_dtype=dt)
+    big = torch.full((M, N + 3 * pad), 3.0, dtype=dt, device="cuda")
+    view = big[:, pad:pad + N]  # base +16 B, pitch (N + 3 pad) elements = 16 mod 32 bytes
+    F.gemm_blockscaled(qa, sa, qb, sb, d=view)
+    assert torch.equal(view, ref)
+    assert (big[:, :pad] == 3).all() and (big[:, pad + N:] == 3).all()
+    _full_check(view, qa, sa, qb, sb, out)
+
+
 def test_exact_integer_inputs(F):
     """Integer entries |v| <= 16 with one +-448 per tile: every scale is 1 and
     every partial sum is an integer below 2^24, so the result must equal int64
