@@ -11,9 +11,11 @@ quantize A [8192][7168] bf16 per 1x128 tile, quantize W [7168][7168] bf16 per
 [8192][7168]. Inputs are seeded synthetic tensors (0.1% x50 outliers in A),
 resident in HBM; every step streams more than the 126 MB L2 (no extra flush).
 
-Each library call of a step is captured once into a CUDA graph (after the
-warm-up) and the timed steps replay those graphs back to back, with CUDA
-events around every call on the launching stream. One JSON line is printed by
+The K timed steps are captured (after the warm-up) into one CUDA graph in which
+an external event-record node brackets every library call, and that graph is
+replayed once between two CUDA events on the launching stream: the step loop
+pays no per-call launch or host overhead, and each call's device time comes
+from its own pair of event nodes. One JSON line is printed by
 rank 0: `value` = GEMM flops (2MNK) of all steps on all ranks / the
 max-over-ranks device time of the K timed steps (the quantizers' time counts
 against it). `roofline` is for the dominant kernel. `e2e` repeats the step
@@ -428,21 +430,61 @@ def run_cpu_baseline(wl):
             "kind": "oracle", "sample": what, "seconds": round(dt, 3)}
 
 
-def capture_graphs(torch, calls):
-    """One CUDA graph per library call (after warm-up); None if capture fails."""
-    graphs = []
+class _Events:
+    """CUDA events recorded as external nodes of a captured graph (so that their
+    timestamps are taken when the graph runs), through the runtime bindings."""
+
+    def __init__(self):
+        from cuda.bindings import runtime as rt
+        self.rt = rt
+
+    def new(self):
+        err, ev = self.rt.cudaEventCreateWithFlags(self.rt.cudaEventDefault)
+        if err != self.rt.cudaError_t.cudaSuccess:
+            raise RuntimeError(f"cudaEventCreateWithFlags: {err}")
+        return ev
+
+    def record(self, ev, stream_handle: int):
+        err, = self.rt.cudaEventRecordWithFlags(ev, self.rt.cudaStream_t(stream_handle),
+                                                self.rt.cudaEventRecordExternal)
+        if err != self.rt.cudaError_t.cudaSuccess:
+            raise RuntimeError(f"cudaEventRecordWithFlags: {err}")
+
+    def elapsed_ms(self, a, b) -> float:
+        err, ms = self.rt.cudaEventElapsedTime(a, b)
+        if err != self.rt.cudaError_t.cudaSuccess:
+            raise RuntimeError(f"cudaEventElapsedTime: {err}")
+        return ms
+
+    def destroy(self, evs):
+        for ev in evs:
+            self.rt.cudaEventDestroy(ev)
+
+
+def capture_steps(torch, calls, pre, steps):
+    """All `steps` timed steps in one CUDA graph, each library call between two
+    external event-record nodes. Returns (graph, events, per-step event pairs) or
+    None if capture fails (the caller then times eager launches)."""
     try:
+        E = _Events()
+        n = len(calls)
+        evs = [[E.new() for _ in range(2 * n)] for _ in range(steps)]
         side = torch.cuda.Stream()
         side.wait_stream(torch.cuda.current_stream())
         with torch.cuda.stream(side):
-            for c in calls:
-                g = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(g, stream=side):
-                    c()
-                graphs.append(g)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=side):
+                h = side.cuda_stream
+                for s in range(steps):
+                    for i, c in enumerate(calls):
+                        if pre:
+                            pre()
+                        E.record(evs[s][2 * i], h)
+                        c()
+                        E.record(evs[s][2 * i + 1], h)
         torch.cuda.current_stream().wait_stream(side)
         torch.cuda.synchronize()
-        return graphs
+        return g, E, evs
     except Exception as e:  # fall back to eager launches
         print(f"# CUDA graph capture failed ({e!r}); timing eager launches", file=sys.stderr)
         return None
@@ -473,34 +515,45 @@ def run_ours(args):
                 pre()
             c()
     torch.cuda.synchronize()
-    graphs = capture_graphs(torch, calls)
-    launch = [g.replay for g in graphs] if graphs else calls
+    captured = capture_steps(torch, calls, pre, args.steps)
     stream = torch.cuda.current_stream()
-    for f in launch:  # one untimed pass of the replays
-        f()
-    n = len(launch)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * n)] for _ in range(args.steps)]
+    n = len(calls)
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if captured:
+        graph, E, gevs = captured
+        graph.replay()  # untimed: uploads the graph
+        torch.cuda.synchronize()
+    else:
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * n)]
+               for _ in range(args.steps)]
 
     clocks = ClockSampler(local)
     clocks.start()
     barrier()
     torch.cuda.synchronize()
     t_start.record(stream)
-    for s in range(args.steps):
-        for i, f in enumerate(launch):
-            if pre:
-                pre()
-            evs[s][2 * i].record(stream)
-            f()
-            evs[s][2 * i + 1].record(stream)
+    if captured:
+        graph.replay()
+    else:
+        for s in range(args.steps):
+            for i, f in enumerate(calls):
+                if pre:
+                    pre()
+                evs[s][2 * i].record(stream)
+                f()
+                evs[s][2 * i + 1].record(stream)
     t_end.record(stream)
     torch.cuda.synchronize()
     barrier()
     clk = clocks.stop()
 
-    per_call_ms = [statistics.mean(evs[s][2 * i].elapsed_time(evs[s][2 * i + 1])
-                                   for s in range(args.steps)) for i in range(n)]
+    if captured:
+        per_call_ms = [statistics.mean(E.elapsed_ms(gevs[s][2 * i], gevs[s][2 * i + 1])
+                                       for s in range(args.steps)) for i in range(n)]
+        E.destroy([e for row in gevs for e in row])
+    else:
+        per_call_ms = [statistics.mean(evs[s][2 * i].elapsed_time(evs[s][2 * i + 1])
+                                       for s in range(args.steps)) for i in range(n)]
     if pre:  # only the timed calls count; the flushes are not work
         local_s = sum(per_call_ms) / 1e3 * args.steps
         value, t_max = aggregate(local_s, wl.bytes * args.steps, rmax, rsum)
@@ -564,7 +617,8 @@ def run_ours(args):
             "config": {"workload": wl.name, **wl.config,
                        "l2": ("L2 refilled with clean lines before each call" if pre else
                               "inputs larger than L2 (no flush)"),
-                       "launch": "CUDA graph replay per library call" if graphs else "eager",
+                       "launch": ("one CUDA graph of all timed steps, event nodes around each "
+                                  "call" if captured else "eager"),
                        "parallelism": f"{world} independent replica(s), one per GPU"},
             "roofline": roof, "kernels": kern, "e2e": e2e, "cpu_baseline": cpu,
             "gpu_launches": n * args.steps, "clocks": clk,
