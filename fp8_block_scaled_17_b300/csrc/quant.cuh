@@ -105,37 +105,56 @@ __global__ void __launch_bounds__(256) quant_rows_1x128_kernel(
   extern __shared__ __align__(16) uint8_t smem[];
   const int hw = threadIdx.x >> 4;
   const int l = threadIdx.x & 15;
-  const int64_t n_units = ((M + kRowUnitRows - 1) / kRowUnitRows) * KB;
   const uint32_t ring = smem_u32(smem);
 
-  // unit u -> rows (u / KB) * 64 .., K-block u % KB
-  auto issue = [&](int64_t u, int stage) {
-    if (u < n_units) {
-      const int64_t row0 = (u / KB) * kRowUnitRows;
-      const int kb = static_cast<int>(u % KB);
+  // Unit u covers rows (u / KB) * 64 .. and K-block u % KB. A CTA visits units
+  // u0, u0 + G, ...: the (row block, K-block) pair of its next unit is advanced
+  // by (G / KB, G % KB) with a carry, so no 64-bit division runs per unit.
+  struct Pos {
+    int64_t rb;
+    int kb;
+  };
+  const int64_t G = gridDim.x;
+  const int64_t g_rb = G / KB;
+  const int g_kb = static_cast<int>(G % KB);
+  auto advance = [&](Pos& q) {
+    q.rb += g_rb;
+    q.kb += g_kb;
+    if (q.kb >= KB) {
+      q.kb -= KB;
+      ++q.rb;
+    }
+  };
+  const int64_t n_rb = (M + kRowUnitRows - 1) / kRowUnitRows;
+
+  auto issue = [&](const Pos& q, int stage) {
+    if (q.rb < n_rb) {
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int rr = hw + 16 * i;
-        const int64_t r = row0 + rr;
+        const int64_t r = q.rb * kRowUnitRows + rr;
         const bool ok = r < M;
-        const __nv_bfloat16* src = ok ? x + r * ldx + kb * 128 + l * 8 : x;
+        const __nv_bfloat16* src = ok ? x + r * ldx + q.kb * 128 + l * 8 : x;
         cp_async_16(ring + ((stage * kRowUnitRows + rr) * 16 + l) * 16, src, ok ? 16u : 0u);
       }
     }
     cp_async_commit();
   };
 
-  const int64_t u0 = blockIdx.x, G = gridDim.x;
+  Pos cur{static_cast<int64_t>(blockIdx.x) / KB, static_cast<int>(blockIdx.x % KB)};
+  Pos nxt = cur;
 #pragma unroll
-  for (int s = 0; s < kRowStages - 1; ++s) issue(u0 + s * G, s);
-  for (int64_t k = 0;; ++k) {
-    const int64_t u = u0 + k * G;
-    if (u >= n_units) break;
-    issue(u + (kRowStages - 1) * G, static_cast<int>((k + kRowStages - 1) % kRowStages));
-    cp_async_wait<kRowStages - 1>();  // this thread's chunks of unit u have landed
+  for (int s = 0; s < kRowStages - 1; ++s) {
+    issue(nxt, s);
+    advance(nxt);
+  }
+  for (int64_t k = 0; cur.rb < n_rb; ++k) {
+    issue(nxt, static_cast<int>((k + kRowStages - 1) % kRowStages));
+    advance(nxt);
+    cp_async_wait<kRowStages - 1>();  // this thread's chunks of the current unit have landed
     const int stage = static_cast<int>(k % kRowStages);
-    const int64_t row0 = (u / KB) * kRowUnitRows;
-    const int kb = static_cast<int>(u % KB);
+    const int64_t row0 = cur.rb * kRowUnitRows;
+    const int kb = cur.kb;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int rr = hw + 16 * i;
@@ -163,6 +182,7 @@ __global__ void __launch_bounds__(256) quant_rows_1x128_kernel(
         if (l == 0) sa[static_cast<int64_t>(kb) * M + r] = ts.s;
       }
     }
+    advance(cur);
   }
   cp_async_wait<0>();
 }
