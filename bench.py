@@ -2,7 +2,7 @@
 """Benchmark of the block-scaled FP8 hot path on B300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload dense_fwd|square|moe|wgrad|ksweep|quant]
+                    [--workload dense_fwd|square|dgrad|moe|wgrad|ksweep|quant]
                     [--legs device,e2e,cpu]
 
 Default workload (one "step" = the whole forward hot path of an FP8 Linear):
@@ -64,7 +64,7 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="dense_fwd",
-                    choices=["dense_fwd", "square", "moe", "wgrad", "ksweep", "quant"])
+                    choices=["dense_fwd", "square", "dgrad", "moe", "wgrad", "ksweep", "quant"])
     ap.add_argument("--legs", default="device,e2e,cpu",
                     help="measurement legs to run: device (always), e2e, cpu")
     a = ap.parse_args(argv)
@@ -257,6 +257,38 @@ class MoeGrouped(Workload):
                 lambda: F.grouped_gemm(self.qa, self.sa, self.offs, self.qb, self.sb, d=self.d)]
 
 
+class Dgrad(Workload):
+    """quant_act(dY) -> quant_w(W, [K][N] layout) -> GEMM: dX = dY . W^T, bf16."""
+
+    def __init__(self, problem, device):
+        import torch
+        from fp8_block_scaled_17_b300 import fp8q as F
+        self.F, self.torch, self.p = F, torch, problem
+        T, Cin, Cout = problem.T, problem.Cin, problem.Cout
+        dy, w = problem.make()
+        self.dy, self.w = dy.to(device), w.to(device)
+        self.qa = torch.empty((T, Cout), dtype=torch.uint8, device=device)
+        self.sa = torch.empty((Cout // 128, T), dtype=torch.float32, device=device)
+        self.qb = torch.empty((Cin, Cout), dtype=torch.uint8, device=device)
+        self.sb = torch.empty((Cout // 128, Cin // 128), dtype=torch.float32, device=device)
+        self.d = torch.empty((T, Cin), dtype=torch.bfloat16, device=device)
+        self.name = (f"dense Linear input gradient: dY [{T}][{Cout}] bf16 quantized 1x128, "
+                     f"W [{Cin}][{Cout}] bf16 quantized 128x128 in its own layout, "
+                     f"dX = dY W^T block-scaled FP8 GEMM promoted every 128 K, bf16 dX [{T}][{Cin}]")
+        self.flops = problem.flops
+        self.kernels = [("quant_act_1x128", "hbm", T * Cout * (2 + 1 + 4 / 128)),
+                        ("quant_w_128x128_kn", "hbm", Cin * Cout * (2 + 1 + 4 / 16384)),
+                        ("gemm_blockscaled", "tensor", problem.flops)]
+        self.config = {"T": T, "Cin": Cin, "Cout": Cout, "out": "bf16", "a_scale": "1x128",
+                       "b_scale": "128x128 ([K][N] layout)", "promotion_interval": 128}
+
+    def calls(self):
+        F = self.F
+        return [lambda: F.quant_act_1x128(self.dy, q=self.qa, sa=self.sa),
+                lambda: F.quant_w_128x128(self.w, q=self.qb, sb=self.sb, kn_layout=True),
+                lambda: F.gemm_blockscaled(self.qa, self.sa, self.qb, self.sb, d=self.d)]
+
+
 class Wgrad(Workload):
     """requant(cached X codes 1x128 -> 128x1) -> quant(dY^T) -> GEMM, FP32 dW."""
 
@@ -379,6 +411,8 @@ def make_workload(name, device):
         return DenseForward(W.DENSE_FWD, device)
     if name == "square":
         return DenseForward(W.SQUARE_8K, device)
+    if name == "dgrad":
+        return Dgrad(W.DgradProblem(), device)
     if name == "moe":
         return MoeGrouped(W.MoeProblem(), device)
     if name == "wgrad":

@@ -33,7 +33,7 @@ struct DeviceInfo {
   int num_sms = 0;
   unsigned* status = nullptr;
   // resident CTAs per SM of the persistent quantizer kernels
-  int occ_rows = 1, occ_cols_bf16 = 1, occ_cols_codes = 1;
+  int occ_rows = 1, occ_cols_bf16 = 1, occ_cols_codes = 1, occ_blocks = 1;
 };
 
 // Dynamic shared memory and occupancy of a persistent quantizer kernel.
@@ -85,7 +85,7 @@ fp8q_status device_info(DeviceInfo** out) {
       d.gemm256_ok = fa256.numRegs == kLaunchRegs && fa256.maxThreadsPerBlock >= kThreads;
       using namespace fp8q;
       const int rs = kRowSmemBytes, cs0 = col_smem_bytes<0>(), cs1 = col_smem_bytes<1>();
-      d.occ_rows = d.occ_cols_bf16 = d.occ_cols_codes = 1;
+      d.occ_rows = d.occ_cols_bf16 = d.occ_cols_codes = d.occ_blocks = 1;
       if (!setup_quant_kernel(quant_rows_1x128_kernel<false>, rs, &d.occ_rows) ||
           !setup_quant_kernel(quant_rows_1x128_kernel<true>, rs, &d.occ_rows) ||
           !setup_quant_kernel(quant_cols_kernel<0, false, false>, cs0, &d.occ_cols_bf16) ||
@@ -93,7 +93,9 @@ fp8q_status device_info(DeviceInfo** out) {
           !setup_quant_kernel(quant_cols_kernel<0, true, false>, cs0, &d.occ_cols_bf16) ||
           !setup_quant_kernel(quant_cols_kernel<0, true, true>, cs0, &d.occ_cols_bf16) ||
           !setup_quant_kernel(quant_cols_kernel<1, false, false>, cs1, &d.occ_cols_codes) ||
-          !setup_quant_kernel(quant_cols_kernel<1, false, true>, cs1, &d.occ_cols_codes))
+          !setup_quant_kernel(quant_cols_kernel<1, false, true>, cs1, &d.occ_cols_codes) ||
+          !setup_quant_kernel(quant_blocks_kn_kernel<false>, kBlkSmemBytes, &d.occ_blocks) ||
+          !setup_quant_kernel(quant_blocks_kn_kernel<true>, kBlkSmemBytes, &d.occ_blocks))
         return FP8Q_ERR_CUDA;
       void* addr = nullptr;
       if (cudaGetSymbolAddress(&addr, g_device_status) != cudaSuccess) return FP8Q_ERR_CUDA;
@@ -262,7 +264,8 @@ FP8Q_API fp8q_status fp8q_quant_act_1x128(const void* x, int64_t M, int64_t K, i
 
 FP8Q_API fp8q_status fp8q_quant_w_128x128(const void* w, int64_t K, int64_t N, uint8_t* q,
                                           float* sb, unsigned flags, fp8q_stream_t stream) {
-  if (flags & ~static_cast<unsigned>(FP8Q_POW2_SCALE)) return FP8Q_ERR_INVALID_ARG;
+  if (flags & ~static_cast<unsigned>(FP8Q_POW2_SCALE | FP8Q_W_KN_LAYOUT))
+    return FP8Q_ERR_INVALID_ARG;
   if (K <= 0 || N <= 0 || K % 128 || N % 128) return FP8Q_ERR_SHAPE;
   if (K / 128 >= (1ll << 31) || N / 128 >= (1ll << 31)) return FP8Q_ERR_SHAPE;
   if (!w || !q || !sb) return FP8Q_ERR_INVALID_ARG;
@@ -270,6 +273,15 @@ FP8Q_API fp8q_status fp8q_quant_w_128x128(const void* w, int64_t K, int64_t N, u
   DeviceInfo* dev = nullptr;
   if (fp8q_status st = device_info(&dev)) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (flags & FP8Q_W_KN_LAYOUT) {
+    const unsigned grid = persistent_grid((N / 128) * (K / 128), dev->num_sms, dev->occ_blocks);
+    const __nv_bfloat16* wb = static_cast<const __nv_bfloat16*>(w);
+    if (flags & FP8Q_POW2_SCALE)
+      fp8q::quant_blocks_kn_kernel<true><<<grid, 256, fp8q::kBlkSmemBytes, s>>>(wb, K, N, q, sb);
+    else
+      fp8q::quant_blocks_kn_kernel<false><<<grid, 256, fp8q::kBlkSmemBytes, s>>>(wb, K, N, q, sb);
+    return launch_status();
+  }
   const unsigned grid = persistent_grid((N / 128) * (K / 128), dev->num_sms, dev->occ_cols_bf16);
   const int smem = fp8q::col_smem_bytes<0>();
   if (flags & FP8Q_POW2_SCALE)

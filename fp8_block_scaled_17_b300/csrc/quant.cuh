@@ -346,18 +346,25 @@ __global__ void __launch_bounds__(256, 2) quant_cols_kernel(
         v[i] = units[r * 16 + (cg ^ rg)];
         sr[i] = srow[r];
       }
-      // value in row i, column e: RN32(dec(code) * s_row)
-      auto val = [&](int i, int e) {
-        const uint32_t wd = e < 4 ? v[i].x : v[i].y;
-        const float2 d = dec2((wd >> (8 * (e & 2))) & 0xFFFFu);
-        return __fmul_rn((e & 1) ? d.y : d.x, sr[i]);
-      };
+      // x[i][e] = RN32(dec(code) * s_row) of row 8*rg + i, column 8*cg + e,
+      // decoded once and kept in registers for the max-abs and the quantization
+      float x[8][8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+#pragma unroll
+        for (int pr = 0; pr < 4; ++pr) {
+          const uint32_t wd = pr < 2 ? v[i].x : v[i].y;
+          const float2 d = dec2((wd >> (16 * (pr & 1))) & 0xFFFFu);
+          x[i][2 * pr] = __fmul_rn(d.x, sr[i]);
+          x[i][2 * pr + 1] = __fmul_rn(d.y, sr[i]);
+        }
+      }
       float a[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         a[e] = 0.0f;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) a[e] = fmaxf(a[e], fabsf(val(i, e)));
+        for (int i = 0; i < 8; ++i) a[e] = fmaxf(a[e], fabsf(x[i][e]));
         // the 16 lanes with this column group hold all 128 rows
 #pragma unroll
         for (int o = 1; o <= 8; o <<= 1) a[e] = fmaxf(a[e], __shfl_xor_sync(0xffffffffu, a[e], o));
@@ -368,10 +375,95 @@ __global__ void __launch_bounds__(256, 2) quant_cols_kernel(
         const int64_t c = c0 + 8 * cg + e;
         if (rg == 0) s_out[rb * Cc + c] = ts.s;
         uint2 o;
-        o.x = quant4(ts, val(0, e), val(1, e), val(2, e), val(3, e));
-        o.y = quant4(ts, val(4, e), val(5, e), val(6, e), val(7, e));
+        o.x = quant4(ts, x[0][e], x[1][e], x[2][e], x[3][e]);
+        o.y = quant4(ts, x[4][e], x[5][e], x[6][e], x[7][e]);
         *reinterpret_cast<uint2*>(out + c * ldo + r0 + 8 * rg) = o;
       }
+    }
+  }
+  cp_async_wait<0>();
+}
+
+// -------------------------------------------------------------------------
+// 128x128 blocks kept in the input's own layout: In[K][N] bf16 -> codes
+// Out[K][N] and one scale per block at s_out[cb * (K/128) + rb] ([N/128][K/128]):
+// the weight as the B operand of dX = dY * W^T, which contracts over N.
+// Persistent CTAs walk the blocks, streaming the next ones into a shared-memory
+// ring with cp.async; a half-warp owns one 128-element row segment at a time
+// (16 lanes x 8 values), so loads are whole 256-byte row segments and code
+// stores whole 128-byte ones. The block max-abs is reduced over the CTA.
+// -------------------------------------------------------------------------
+constexpr int kBlkStages = 3;
+constexpr int kBlkTileBytes = 128 * 256;  // one bf16 block
+constexpr int kBlkSmemBytes = kBlkStages * kBlkTileBytes;
+
+template <bool kPow2>
+__global__ void __launch_bounds__(256, 2) quant_blocks_kn_kernel(
+    const __nv_bfloat16* __restrict__ in, int64_t K, int64_t N, uint8_t* __restrict__ out,
+    float* __restrict__ s_out) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  __shared__ float red[8];
+  const int t = threadIdx.x;
+  const int lane = t & 31, warp = t >> 5;
+  const int hw = t >> 4, l = t & 15;
+  const int64_t ncb = N / 128, nrb = K / 128;
+  const int64_t n_tiles = ncb * nrb;
+  const uint32_t ring = smem_u32(smem);
+
+  // block u -> row block u / ncb, column block u % ncb (one division per 16384 values)
+  auto issue = [&](int64_t u, int stage) {
+    if (u < n_tiles) {
+      const int64_t rb = u / ncb, cb = u % ncb;
+      const __nv_bfloat16* src = in + rb * 128 * N + cb * 128 + l * 8;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int r = hw + 16 * i;
+        cp_async_16(ring + stage * kBlkTileBytes + (r * 16 + l) * 16, src + r * N, 16u);
+      }
+    }
+    cp_async_commit();
+  };
+
+  const int64_t u0 = blockIdx.x, G = gridDim.x;
+#pragma unroll
+  for (int st = 0; st < kBlkStages - 1; ++st) issue(u0 + st * G, st);
+  for (int64_t k = 0;; ++k) {
+    const int64_t u = u0 + k * G;
+    if (u >= n_tiles) break;
+    __syncthreads();  // the buffer the next issue overwrites, and red[], are free
+    issue(u + (kBlkStages - 1) * G, static_cast<int>((k + kBlkStages - 1) % kBlkStages));
+    cp_async_wait<kBlkStages - 1>();
+    __syncthreads();  // block u has landed, all threads' chunks
+    const int stage = static_cast<int>(k % kBlkStages);
+    const uint4* tile = reinterpret_cast<const uint4*>(smem + stage * kBlkTileBytes);
+    const int64_t rb = u / ncb, cb = u % ncb;
+
+    uint4 v[8];  // rows hw + 16 i, columns 8 l .. 8 l + 7
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = tile[(hw + 16 * i) * 16 + l];
+    float m = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) m = fmaxf(m, fmaxf(fabsf(bf16_lo(w[j])), fabsf(bf16_hi(w[j]))));
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (lane == 0) red[warp] = m;
+    __syncthreads();
+    float bm = red[0];
+#pragma unroll
+    for (int w2 = 1; w2 < 8; ++w2) bm = fmaxf(bm, red[w2]);
+    const TileScale<kPow2> ts(bm);
+    if (t == 0) s_out[cb * nrb + rb] = ts.s;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+      uint2 o;
+      o.x = quant4(ts, bf16_lo(w[0]), bf16_hi(w[0]), bf16_lo(w[1]), bf16_hi(w[1]));
+      o.y = quant4(ts, bf16_lo(w[2]), bf16_hi(w[2]), bf16_lo(w[3]), bf16_hi(w[3]));
+      *reinterpret_cast<uint2*>(out + (rb * 128 + hw + 16 * i) * N + cb * 128 + l * 8) = o;
     }
   }
   cp_async_wait<0>();

@@ -23,6 +23,7 @@ TRANSPOSED_INPUT = 2
 SCALE_B_1x128 = 4
 NO_PROMOTION = 8
 OUT_BF16 = 16
+W_KN_LAYOUT = 32
 
 EXPORTED = ("fp8q_quant_act_1x128", "fp8q_quant_w_128x128", "fp8q_requant_1x128_to_128x1",
             "fp8q_gemm_blockscaled", "fp8q_grouped_gemm", "fp8q_get_status",
@@ -104,16 +105,18 @@ def quant_act_1x128(x: torch.Tensor, pow2: bool = False, transposed_input: bool 
 
 
 def quant_w_128x128(w: torch.Tensor, pow2: bool = False, q: torch.Tensor | None = None,
-                    sb: torch.Tensor | None = None, stream=None):
-    """w bf16 [K][N] -> (codes u8 [N][K], scales f32 [K/128][N/128])."""
+                    sb: torch.Tensor | None = None, kn_layout: bool = False, stream=None):
+    """w bf16 [K][N] -> (codes u8 [N][K], scales f32 [K/128][N/128]); with
+    kn_layout, the Dgrad operand: (codes u8 [K][N], scales f32 [N/128][K/128])."""
     assert w.dtype == torch.bfloat16 and w.dim() == 2 and w.is_contiguous()
     K, N = w.shape
     if q is None:
-        q = torch.empty((N, K), dtype=torch.uint8, device=w.device)
+        q = torch.empty((K, N) if kn_layout else (N, K), dtype=torch.uint8, device=w.device)
     if sb is None:
-        sb = torch.empty((K // 128, N // 128), dtype=torch.float32, device=w.device)
-    _check(LIB.fp8q_quant_w_128x128(_ptr(w), K, N, _ptr(q), _ptr(sb),
-                                    POW2_SCALE if pow2 else 0, _stream(stream)),
+        sb = torch.empty((N // 128, K // 128) if kn_layout else (K // 128, N // 128),
+                         dtype=torch.float32, device=w.device)
+    flags = (POW2_SCALE if pow2 else 0) | (W_KN_LAYOUT if kn_layout else 0)
+    _check(LIB.fp8q_quant_w_128x128(_ptr(w), K, N, _ptr(q), _ptr(sb), flags, _stream(stream)),
            "fp8q_quant_w_128x128")
     return q, sb
 

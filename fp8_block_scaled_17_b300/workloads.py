@@ -83,6 +83,29 @@ SQUARE_8K = GemmProblem("square 8192x8192x8192", 8192, 8192, 8192, 1.0, 0.02, 0.
                         "bf16")
 
 
+@dataclass
+class DgradProblem:
+    """dX[T][Cin] = dY[T][Cout] . W[Cin][Cout]^T, the input gradient of the dense
+    forward Linear: W is the forward's weight (same seed and shape), dY ~ N(0, 1e-3^2)."""
+    T: int = 8192
+    Cin: int = 7168
+    Cout: int = 7168
+    seed: int = 0
+
+    @property
+    def name(self):
+        return f"dgrad T={self.T} Cin={self.Cin} Cout={self.Cout}"
+
+    def make(self):
+        dy = bf16_normal((self.T, self.Cout), 1e-3, self.seed + 2)
+        w = bf16_normal((self.Cin, self.Cout), 0.02, self.seed + 1)
+        return dy, w
+
+    @property
+    def flops(self) -> float:
+        return 2.0 * self.T * self.Cin * self.Cout
+
+
 def ksweep_problem(K: int) -> GemmProblem:
     return GemmProblem(f"k-sweep 4096x4096x{K}", 4096, 4096, K, 1.0, 1.0, 0.0, 1.0, "f32")
 

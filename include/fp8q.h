@@ -67,7 +67,8 @@ enum {
   FP8Q_TRANSPOSED_INPUT = 2, /* quant_act: x is stored [K][M]                */
   FP8Q_SCALE_B_1x128 = 4,    /* GEMM: B has one scale per (column, K-block)  */
   FP8Q_NO_PROMOTION = 8,     /* GEMM: accumulate all of K in the tensor core */
-  FP8Q_OUT_BF16 = 16         /* GEMM: bf16 output (default float32)          */
+  FP8Q_OUT_BF16 = 16,        /* GEMM: bf16 output (default float32)          */
+  FP8Q_W_KN_LAYOUT = 32      /* quant_w: codes kept [K][N] (Dgrad operand)   */
 };
 
 /*
@@ -89,10 +90,15 @@ fp8q_status fp8q_quant_act_1x128(const void* x, int64_t M, int64_t K, int64_t ld
 /*
  * 128x128 weight-block quantization [WHY-BE].
  * w  : bf16 [K][N] row-major (input channels x output channels), contiguous.
- * q  : uint8 codes [N][K] (transposed: K-major, the GEMM's B operand).
+ * q  : uint8 codes [N][K] (transposed: K-major, the GEMM's B operand for the
+ *      forward product Y = X W, which contracts over K).
  * sb : float32 [K/128][N/128], one scale per 128x128 block.
+ * FP8Q_W_KN_LAYOUT: the same codes and scales laid out for the input-gradient
+ *      product dX = dY W^T, which contracts over N [FOOLED, Figure 6: the
+ *      Dgrad GEMM of an FP8 Linear]: q is [K][N] (the input's own layout,
+ *      N-major rows) and sb is [N/128][K/128] (sb[nb * (K/128) + kb]).
  * K % 128 == 0 and N % 128 == 0, both > 0. w, q 16-byte aligned.
- * flags: FP8Q_POW2_SCALE.
+ * flags: FP8Q_POW2_SCALE | FP8Q_W_KN_LAYOUT.
  */
 fp8q_status fp8q_quant_w_128x128(const void* w, int64_t K, int64_t N, uint8_t* q,
                                  float* sb, unsigned flags, fp8q_stream_t stream);

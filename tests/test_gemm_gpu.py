@@ -80,6 +80,25 @@ def test_output_16b_aligned_only(F, out):
     _full_check(view, qa, sa, qb, sb, out)
 
 
+@pytest.mark.parametrize("T,Cin,Cout", [(300, 384, 512), (256, 256, 1024), (129, 640, 384)])
+def test_dgrad_path(F, T, Cin, Cout):
+    """dX = dY . W^T: dY quantized 1x128 along Cout, W [Cin][Cout] quantized 128x128
+    in the [K][N] layout (B = W itself, contracting over Cout); every output
+    against the oracle run on the oracle's own forward-layout codes, transposed."""
+    dy = W.bf16_normal((T, Cout), 1e-3, seed=T + Cout)
+    w = W.bf16_normal((Cin, Cout), 0.02, seed=Cin + 3 * Cout)
+    qa, sa = F.quant_act_1x128(dy.cuda())
+    qb, sb = F.quant_w_128x128(w.cuda(), kn_layout=True)
+    d = F.gemm_blockscaled(qa, sa, qb, sb, out_dtype=torch.bfloat16)
+    rqa, rsa = O.quant_act_1x128(dy.float().numpy())
+    rqw, rsw = O.quant_w_128x128(w.float().numpy())   # [Cout][Cin], [Cin/128][Cout/128]
+    rqb, rsb = np.ascontiguousarray(rqw.T), np.ascontiguousarray(rsw.T)
+    ref = O.gemm_blockscaled(rqa, rsa, rqb, rsb)
+    na, nb = O.row_col_norms(rqa, rsa, rqb, rsb)
+    assert d.shape == (T, Cin)
+    assert_gemm_close(to_np(d), ref, na, nb, "bf16")
+
+
 def test_exact_integer_inputs(F):
     """Integer entries |v| <= 16 with one +-448 per tile: every scale is 1 and
     every partial sum is an integer below 2^24, so the result must equal int64
@@ -173,6 +192,18 @@ def test_square_8192_full_sampled(F):
     d = F.gemm_blockscaled(qa, sa, qb, sb, out_dtype=torch.bfloat16)
     check_gemm_sampled(to_np(d), qa.cpu().numpy(), sa.cpu().numpy(), qb.cpu().numpy(),
                        sb.cpu().numpy(), _sample_rows(p.M, 40, 1), [0, 31, 63], "bf16")
+
+
+def test_dgrad_full_sampled(F):
+    """Dgrad dX [8192][7168] = dY [8192][7168] . W^T with the forward's W quantized
+    in the [K][N] layout; sampled rows x 128-column blocks against the oracle."""
+    p = W.DgradProblem()
+    dy, w = p.make()
+    qa, sa = F.quant_act_1x128(dy.cuda())
+    qb, sb = F.quant_w_128x128(w.cuda(), kn_layout=True)
+    d = F.gemm_blockscaled(qa, sa, qb, sb, out_dtype=torch.bfloat16)
+    check_gemm_sampled(to_np(d), qa.cpu().numpy(), sa.cpu().numpy(), qb.cpu().numpy(),
+                       sb.cpu().numpy(), _sample_rows(p.T, 40, 2), [0, 29, 55], "bf16")
 
 
 def test_wgrad_full_sampled(F):

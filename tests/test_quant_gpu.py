@@ -94,6 +94,17 @@ def test_quant_w(F, K, N, pow2):
     _assert_same(q, sb, *O.quant_w_128x128(w.float().numpy(), pow2))
 
 
+@pytest.mark.parametrize("K,N,pow2", [(512, 256, False), (384, 640, True), (128, 128, False),
+                                      (256, 1024, True)])
+def test_quant_w_kn_layout(F, K, N, pow2):
+    """The Dgrad operand: the same codes and block scales as the forward layout,
+    laid out [K][N] and [N/128][K/128]."""
+    w = W.bf16_normal((K, N), 0.02, seed=K + 5 * N, outlier_frac=0.001, outlier_scale=50.0)
+    q, sb = F.quant_w_128x128(w.cuda(), pow2, kn_layout=True)
+    rq, rs = O.quant_w_128x128(w.float().numpy(), pow2)
+    _assert_same(q, sb, np.ascontiguousarray(rq.T), np.ascontiguousarray(rs.T))
+
+
 # ----------------------------------------------------------- requant 1x128 -> 128x1
 @pytest.mark.parametrize("T,C,pow2", [(256, 384, True), (384, 256, False), (128, 128, True)])
 def test_requant(F, T, C, pow2):
@@ -112,7 +123,10 @@ def test_quant_dense_forward_full(F):
     qa, sa = F.quant_act_1x128(a.cuda())
     _assert_same(qa, sa, *O.quant_act_1x128(a.float().numpy()))
     qw, sw = F.quant_w_128x128(w.cuda())
-    _assert_same(qw, sw, *O.quant_w_128x128(w.float().numpy()))
+    rq, rs = O.quant_w_128x128(w.float().numpy())
+    _assert_same(qw, sw, rq, rs)
+    qk, sk = F.quant_w_128x128(w.cuda(), kn_layout=True)  # the Dgrad layout of the same weight
+    _assert_same(qk, sk, np.ascontiguousarray(rq.T), np.ascontiguousarray(rs.T))
 
 
 def test_quant_moe_and_wgrad_full_sampled(F):
