@@ -31,18 +31,31 @@ __device__ __forceinline__ uint32_t enc2(float lo, float hi) {
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
   return r;
 }
+// four float32 -> four codes, `a` in the low byte; the two 16-bit halves are
+// joined by a register move rather than shifts
 __device__ __forceinline__ uint32_t enc4(float a, float b, float c, float d) {
-  return enc2(a, b) | (enc2(c, d) << 16);
+  uint32_t r;
+  asm("{\n\t.reg .b16 lo, hi;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n\t"
+      "mov.b32 %0, {lo, hi};\n\t}"
+      : "=r"(r)
+      : "f"(a), "f"(b), "f"(c), "f"(d));
+  return r;
 }
-// two E4M3 codes (low byte first) -> exact float32 values
-__device__ __forceinline__ float2 dec2(uint32_t two_codes) {
-  uint32_t h2;
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(static_cast<uint16_t>(two_codes)));
-  float lo, hi;
-  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}"
-      : "=f"(lo), "=f"(hi)
-      : "r"(h2));
-  return make_float2(lo, hi);
+// four E4M3 codes (low byte first) -> exact float32 values; the word is split
+// into its 16-bit halves by a register move
+__device__ __forceinline__ void dec4(uint32_t w, float& x0, float& x1, float& x2, float& x3) {
+  asm("{\n\t.reg .b16 c0, c1, l0, h0, l1, h1;\n\t.reg .b32 p0, p1;\n\t"
+      "mov.b32 {c0, c1}, %4;\n\t"
+      "cvt.rn.f16x2.e4m3x2 p0, c0;\n\t"
+      "cvt.rn.f16x2.e4m3x2 p1, c1;\n\t"
+      "mov.b32 {l0, h0}, p0;\n\t"
+      "mov.b32 {l1, h1}, p1;\n\t"
+      "cvt.f32.f16 %0, l0;\n\tcvt.f32.f16 %1, h0;\n\t"
+      "cvt.f32.f16 %2, l1;\n\tcvt.f32.f16 %3, h1;\n\t}"
+      : "=f"(x0), "=f"(x1), "=f"(x2), "=f"(x3)
+      : "r"(w));
 }
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
@@ -84,6 +97,39 @@ __device__ __forceinline__ uint32_t quant4(const TileScale<kPow2>& ts, float x0,
                                            float x2, float x3) {
   return enc4(__fmul_rn(x0, ts.f), __fmul_rn(x1, ts.f), __fmul_rn(x2, ts.f),
               __fmul_rn(x3, ts.f));
+}
+
+// Four codes enc(RN32(x_i * f)) with a given quantization factor.
+__device__ __forceinline__ uint32_t quant4f(float f, float x0, float x1, float x2, float x3) {
+  return enc4(__fmul_rn(x0, f), __fmul_rn(x1, f), __fmul_rn(x2, f), __fmul_rn(x3, f));
+}
+
+// Max-abs of 8 columns held as 8 partial maxima by each of the 16 lanes of a
+// half-warp (lane bits 0-3). Each exchange step sends half of the remaining
+// columns and keeps the other half, so 8 shuffles replace 32; afterwards lane l
+// holds the full max of column colmax_col(l) = 4*b3 + 2*b2 + b1 (l and l^1 agree).
+__device__ __forceinline__ int colmax_col(int lane) {
+  return ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1);
+}
+// the lane (same half-warp) whose colmax_col is e
+__device__ __forceinline__ int colmax_src(int lane, int e) {
+  return (lane & 16) | ((e >> 2) << 3) | (((e >> 1) & 1) << 2) | ((e & 1) << 1);
+}
+__device__ __forceinline__ float colmax8(const float (&a)[8], int lane) {
+  const bool b3 = lane & 8, b2 = lane & 4, b1 = lane & 2;
+  float k[4], m[2];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float send = b3 ? a[j] : a[4 + j];
+    k[j] = fmaxf(b3 ? a[4 + j] : a[j], __shfl_xor_sync(0xffffffffu, send, 8));
+  }
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const float send = b2 ? k[j] : k[2 + j];
+    m[j] = fmaxf(b2 ? k[2 + j] : k[j], __shfl_xor_sync(0xffffffffu, send, 4));
+  }
+  float n = fmaxf(b1 ? m[1] : m[0], __shfl_xor_sync(0xffffffffu, b1 ? m[0] : m[1], 2));
+  return fmaxf(n, __shfl_xor_sync(0xffffffffu, n, 1));
 }
 
 // -------------------------------------------------------------------------
@@ -300,38 +346,42 @@ __global__ void __launch_bounds__(256, 2) quant_cols_kernel(
         a[2 * kk] = lo;
         a[2 * kk + 1] = hi;
       }
-      // the 16 lanes with this column group hold all 128 rows
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-#pragma unroll
-        for (int o = 1; o <= 8; o <<= 1) a[e] = fmaxf(a[e], __shfl_xor_sync(0xffffffffu, a[e], o));
-      }
-      if (kBlock) {
+      float fblk = 0.0f;
+      if (kBlock) {  // one max over the thread's 64 values, then over the warp and the CTA
         float m = a[0];
 #pragma unroll
         for (int e = 1; e < 8; ++e) m = fmaxf(m, a[e]);
-        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));  // the warp's two column groups
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
         if (lane == 0) red[warp] = m;
         __syncthreads();
         float bm = red[0];
 #pragma unroll
         for (int w2 = 1; w2 < 8; ++w2) bm = fmaxf(bm, red[w2]);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) a[e] = bm;
-        if (t == 0) s_out[rb * ncb + cb] = TileScale<kPow2>(bm).s;
+        const TileScale<kPow2> ts(bm);
+        if (t == 0) s_out[rb * ncb + cb] = ts.s;
+        fblk = ts.f;
+      }
+      // quantization factor of column e of this thread's column group: one
+      // scale per lane (its colmax8 column), then broadcast
+      float fcol = 0.0f;
+      if (!kBlock) {
+        const TileScale<kPow2> ts(colmax8(a, lane));
+        const int64_t c = c0 + 8 * cg + colmax_col(lane);
+        if ((lane & 1) == 0 && c < Cc) s_out[rb * Cc + c] = ts.s;
+        fcol = ts.f;
       }
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        const TileScale<kPow2> ts(a[e]);
+        const float f = kBlock ? fblk : __shfl_sync(0xffffffffu, fcol, colmax_src(lane, e));
         const int64_t c = c0 + 8 * cg + e;
-        if (!kBlock && rg == 0 && c < Cc) s_out[rb * Cc + c] = ts.s;
         const int kk = e >> 1;
         float xv[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) xv[i] = (e & 1) ? bf16_hi(w[i][kk]) : bf16_lo(w[i][kk]);
         uint2 o;
-        o.x = quant4(ts, xv[0], xv[1], xv[2], xv[3]);
-        o.y = quant4(ts, xv[4], xv[5], xv[6], xv[7]);
+        o.x = quant4f(f, xv[0], xv[1], xv[2], xv[3]);
+        o.y = quant4f(f, xv[4], xv[5], xv[6], xv[7]);
         if (c < Cc) *reinterpret_cast<uint2*>(out + c * ldo + r0 + 8 * rg) = o;
       }
     } else {
@@ -351,13 +401,11 @@ __global__ void __launch_bounds__(256, 2) quant_cols_kernel(
       float x[8][8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
+        float d[8];
+        dec4(v[i].x, d[0], d[1], d[2], d[3]);
+        dec4(v[i].y, d[4], d[5], d[6], d[7]);
 #pragma unroll
-        for (int pr = 0; pr < 4; ++pr) {
-          const uint32_t wd = pr < 2 ? v[i].x : v[i].y;
-          const float2 d = dec2((wd >> (16 * (pr & 1))) & 0xFFFFu);
-          x[i][2 * pr] = __fmul_rn(d.x, sr[i]);
-          x[i][2 * pr + 1] = __fmul_rn(d.y, sr[i]);
-        }
+        for (int e = 0; e < 8; ++e) x[i][e] = __fmul_rn(d[e], sr[i]);
       }
       float a[8];
 #pragma unroll
@@ -365,18 +413,18 @@ __global__ void __launch_bounds__(256, 2) quant_cols_kernel(
         a[e] = 0.0f;
 #pragma unroll
         for (int i = 0; i < 8; ++i) a[e] = fmaxf(a[e], fabsf(x[i][e]));
-        // the 16 lanes with this column group hold all 128 rows
-#pragma unroll
-        for (int o = 1; o <= 8; o <<= 1) a[e] = fmaxf(a[e], __shfl_xor_sync(0xffffffffu, a[e], o));
       }
+      // the 16 lanes with this column group hold all 128 rows: one scale per
+      // lane (its colmax8 column), then the factors are broadcast
+      const TileScale<kPow2> ts(colmax8(a, lane));
+      if ((lane & 1) == 0) s_out[rb * Cc + c0 + 8 * cg + colmax_col(lane)] = ts.s;
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        const TileScale<kPow2> ts(a[e]);
+        const float f = __shfl_sync(0xffffffffu, ts.f, colmax_src(lane, e));
         const int64_t c = c0 + 8 * cg + e;
-        if (rg == 0) s_out[rb * Cc + c] = ts.s;
         uint2 o;
-        o.x = quant4(ts, x[0][e], x[1][e], x[2][e], x[3][e]);
-        o.y = quant4(ts, x[4][e], x[5][e], x[6][e], x[7][e]);
+        o.x = quant4f(f, x[0][e], x[1][e], x[2][e], x[3][e]);
+        o.y = quant4f(f, x[4][e], x[5][e], x[6][e], x[7][e]);
         *reinterpret_cast<uint2*>(out + c * ldo + r0 + 8 * rg) = o;
       }
     }
