@@ -2,7 +2,8 @@
 """Benchmark of the block-scaled FP8 hot path on B300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload dense_fwd|square|dgrad|moe|wgrad|ksweep|quant]
+                    [--workload dense_fwd|square|dgrad|moe|moe_decode|moe_act_grad|
+                                wgrad|ksweep|quant]
                     [--legs device,e2e,cpu]
 
 Default workload (one "step" = the whole forward hot path of an FP8 Linear):
@@ -64,7 +65,8 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="dense_fwd",
-                    choices=["dense_fwd", "square", "dgrad", "moe", "wgrad", "ksweep", "quant"])
+                    choices=["dense_fwd", "square", "dgrad", "moe", "moe_decode", "moe_act_grad",
+                             "wgrad", "ksweep", "quant"])
     ap.add_argument("--legs", default="device,e2e,cpu",
                     help="measurement legs to run: device (always), e2e, cpu")
     a = ap.parse_args(argv)
@@ -222,7 +224,7 @@ class DenseForward(Workload):
 class MoeGrouped(Workload):
     """quant_act(tokens, pow2) -> grouped GEMM over expert-sorted rows."""
 
-    def __init__(self, problem, device):
+    def __init__(self, problem, device, decode=False):
         import torch
         from fp8_block_scaled_17_b300 import fp8q as F
         self.F, self.torch, self.p = F, torch, problem
@@ -243,10 +245,16 @@ class MoeGrouped(Workload):
         for e in range(E):
             F.quant_w_128x128(w[e].to(device), q=self.qb[e], sb=self.sb[e])
         self.d = torch.empty((problem.rows, N), dtype=torch.bfloat16, device=device)
-        self.name = problem.name
+        self.name = getattr(self, "name", problem.name)
         self.flops = problem.flops
+        gemm = ("grouped_gemm", "tensor", problem.flops)
+        if decode:  # weight-bandwidth bound: algorithmic bytes of codes, scales and D
+            gemm = ("grouped_gemm", "hbm",
+                    E * N * K + problem.rows * K + problem.rows * N * 2
+                    + E * (K // 128) * (N // 128) * 4 + (K // 128) * problem.rows * 4)
+            self.name = problem.name + " (decode: few rows per expert, weight-bandwidth bound)"
         self.kernels = [("quant_act_1x128_pow2", "hbm", problem.tokens * K * (2 + 1 + 4 / 128)),
-                        ("grouped_gemm", "tensor", problem.flops)]
+                        gemm]
         self.config = {"tokens": problem.tokens, "experts": E, "topk": problem.topk,
                        "rows": problem.rows, "K": K, "N": N,
                        "expert_rows": (offs[1:] - offs[:-1]).tolist(), "out": "bf16"}
@@ -255,6 +263,28 @@ class MoeGrouped(Workload):
         F = self.F
         return [lambda: F.quant_act_1x128(self.x, True, q=self.qx, sa=self.sx),
                 lambda: F.grouped_gemm(self.qa, self.sa, self.offs, self.qb, self.sb, d=self.d)]
+
+
+class MoeActGrad(Workload):
+    """Power-of-two 1x128 quantization of the MoE down-projection input gradient."""
+
+    def __init__(self, problem, device):
+        import torch
+        from fp8_block_scaled_17_b300 import fp8q as F
+        self.F, self.torch = F, torch
+        R, N = problem.rows, problem.N
+        self.g = problem.make().to(device)
+        self.q = torch.empty((R, N), dtype=torch.uint8, device=device)
+        self.s = torch.empty((N // 128, R), dtype=torch.float32, device=device)
+        self.name = problem.name + " quantized 1x128 with power-of-two scales"
+        self.bytes = R * N * (2 + 1 + 4 / 128)
+        self.flops = 0.0
+        self.kernels = [("quant_act_1x128_pow2", "hbm", self.bytes)]
+        self.config = {"rows": R, "N": N, "scale": "1x128 pow2"}
+
+    def calls(self):
+        F = self.F
+        return [lambda: F.quant_act_1x128(self.g, True, q=self.q, sa=self.s)]
 
 
 class Dgrad(Workload):
@@ -415,6 +445,10 @@ def make_workload(name, device):
         return Dgrad(W.DgradProblem(), device)
     if name == "moe":
         return MoeGrouped(W.MoeProblem(), device)
+    if name == "moe_decode":
+        return MoeGrouped(W.MOE_DECODE, device, decode=True)
+    if name == "moe_act_grad":
+        return MoeActGrad(W.MoeActGradProblem(), device)
     if name == "wgrad":
         return Wgrad(W.WgradProblem(), device)
     if name == "quant":
@@ -590,6 +624,10 @@ def run_ours(args):
                                        for s in range(args.steps)) for i in range(n)]
     if pre:  # only the timed calls count; the flushes are not work
         local_s = sum(per_call_ms) / 1e3 * args.steps
+        value, t_max = aggregate(local_s, wl.bytes * args.steps, rmax, rsum)
+        value, unit = value / 1e9, "GB/s"
+    elif not wl.flops:  # a quantizer-only step
+        local_s = t_start.elapsed_time(t_end) / 1e3
         value, t_max = aggregate(local_s, wl.bytes * args.steps, rmax, rsum)
         value, unit = value / 1e9, "GB/s"
     else:

@@ -154,6 +154,28 @@ class MoeProblem:
         return 2.0 * self.rows * self.N * self.K
 
 
+# Small-M MoE decode: 256 tokens x top-9 over 16 experts (at most 256 rows per
+# expert); reading the expert weights dominates.
+MOE_DECODE = MoeProblem(tokens=256)
+
+
+@dataclass
+class MoeActGradProblem:
+    """Gradient of the MoE down-projection input, [tokens x topk][N] bf16 ~ N(0, 1e-3^2),
+    in expert order: quantized 1x128 along N with power-of-two scales before the
+    down-projection's backward GEMMs."""
+    rows: int = 16384 * 9
+    N: int = 2048
+    seed: int = 0
+
+    @property
+    def name(self):
+        return f"moe activation gradient [{self.rows}][{self.N}]"
+
+    def make(self):
+        return bf16_normal((self.rows, self.N), 1e-3, self.seed + 5)
+
+
 @dataclass
 class WgradProblem:
     """dW[Cin][Cout] = X^T . dY over T tokens."""

@@ -49,11 +49,7 @@ def test_grouped_small(F, sizes, out):
             assert_gemm_close(dn[r0:r1], ref[r0:r1], na, nb, out)
 
 
-def test_moe_full_sampled(F):
-    """16 experts, 16384 tokens x top-9 with Zipf(1.1) loads (147456 rows),
-    K = 7168, N = 2048, pow2 1x128 activation scales, bf16 out: the bench's
-    grouped workload. Sampled rows of every expert against the oracle."""
-    p = W.MoeProblem()
+def _moe_check_sampled(F, p, rows_per_expert):
     x, w, rows, offs = p.make()
     qx, sx = F.quant_act_1x128(x.cuda(), True)            # quantize before dispatch
     rows_d = rows.cuda()
@@ -72,8 +68,29 @@ def test_moe_full_sampled(F):
     cols = np.concatenate([np.arange(0, 128), np.arange(p.N - 128, p.N)])
     for e in range(p.experts):
         r0, r1 = int(o[e]), int(o[e + 1])
-        pick = np.unique(np.concatenate([g.integers(r0, r1, 6), [r0, r1 - 1]]))
+        if r1 == r0:
+            continue
+        if rows_per_expert is None:
+            pick = np.arange(r0, r1)
+        else:
+            pick = np.unique(np.concatenate([g.integers(r0, r1, rows_per_expert), [r0, r1 - 1]]))
         sbe = sb_n[e][:, [0, p.N // 128 - 1]]
         ref = O.gemm_blockscaled(qa_n[pick], sa_n[:, pick], qb_n[e][cols], sbe)
         na, nb = O.row_col_norms(qa_n[pick], sa_n[:, pick], qb_n[e][cols], sbe)
         assert_gemm_close(dn[np.ix_(pick, cols)], ref, na, nb, "bf16")
+
+
+def test_moe_full_sampled(F):
+    """16 experts, 16384 tokens x top-9 with Zipf(1.1) loads (147456 rows),
+    K = 7168, N = 2048, pow2 1x128 activation scales, bf16 out: the bench's
+    grouped workload. Sampled rows of every expert against the oracle."""
+    _moe_check_sampled(F, W.MoeProblem(), 6)
+
+
+def test_moe_decode_all_rows(F):
+    """Small-M decode: 256 tokens x top-9 over 16 experts (at most 256 rows per
+    expert): every row of every expert, first and last 128 columns."""
+    p = W.MOE_DECODE
+    _, _, _, offs = p.make()
+    assert int((offs[1:] - offs[:-1]).max()) <= 256
+    _moe_check_sampled(F, p, None)

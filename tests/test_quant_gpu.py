@@ -153,3 +153,17 @@ def test_quant_moe_and_wgrad_full_sampled(F):
     qd, sd = F.quant_act_1x128(dy.cuda(), False, transposed_input=True)
     rq3, rs3 = O.quant_act_1x128(dy[:, chans].float().numpy().T, False)
     assert (_np(qd)[chans] == rq3).all() and (bits(_np(sd)[:, chans]) == bits(rs3)).all()
+
+
+def test_moe_activation_gradient_pow2_sampled(F):
+    """The MoE down-projection input gradient [147456][2048] ~ N(0, 1e-3^2),
+    1x128 with power-of-two scales, as timed by `bench.py --workload
+    moe_act_grad`: sampled rows (codes and scales) bit-exact."""
+    p = W.MoeActGradProblem()
+    g = p.make()
+    q, s = F.quant_act_1x128(g.cuda(), True)
+    rows = np.unique(np.concatenate([np.random.default_rng(3).choice(p.rows, 48, replace=False),
+                                     [0, 1, p.rows - 1]]))
+    idx = torch.as_tensor(rows, device="cuda")
+    rq, rs = O.quant_act_1x128(g[torch.as_tensor(rows)].float().numpy(), True)
+    _assert_same(q.index_select(0, idx), s.index_select(1, idx), rq, rs)
