@@ -166,6 +166,40 @@ def test_no_promotion_variant(F, K):
     assert err_n < 0.1  # same codes, only the accumulation differs
 
 
+def test_tile_n_128_variant(F, monkeypatch):
+    """FP8Q_GEMM_TILE_N=128 selects 128x128 CTA tiles (four TMEM buffers, a
+    deeper stage ring): the same results as the default tile, bit for bit, on
+    ragged shapes, 1x128 B scales, no promotion and a grouped call."""
+    cases = []
+    qa, sa, qb, sb = _quantized_problem(F, 300, 384, 640, seed=101)
+    cases.append(lambda: F.gemm_blockscaled(qa, sa, qb, sb, out_dtype=torch.bfloat16))
+    x = W.bf16_normal((512, 200), 1.0, seed=102).cuda()     # [tokens][channels]
+    dy = W.bf16_normal((512, 384), 1e-3, seed=103).cuda()
+    qx, sx = F.quant_act_1x128(x, transposed_input=True)     # [200][512], 1x128 along tokens
+    qd, sd = F.quant_act_1x128(dy, transposed_input=True)    # [384][512]
+    cases.append(lambda: F.gemm_blockscaled(qx, sx, qd, sd, out_dtype=torch.float32,
+                                            scale_b_1x128=True))
+    qk, sk = F.quant_act_1x128(W.ksweep_operand(256, 1024, 104).cuda(), True)
+    cases.append(lambda: F.gemm_blockscaled(qk, sk, qk, sk, scale_b_1x128=True,
+                                            no_promotion=True))
+    offs = torch.tensor([0, 3, 3, 133, 300], dtype=torch.int32, device="cuda")
+    qe = torch.empty((4, 256, 640), dtype=torch.uint8, device="cuda")
+    se = torch.empty((4, 5, 2), dtype=torch.float32, device="cuda")
+    for e in range(4):
+        F.quant_w_128x128(W.bf16_normal((640, 256), 0.02, seed=110 + e).cuda(), q=qe[e], sb=se[e])
+    cases.append(lambda: F.grouped_gemm(qa, sa, offs, qe, se, out_dtype=torch.bfloat16))
+
+    monkeypatch.delenv("FP8Q_GEMM_TILE_N", raising=False)
+    ref = [c() for c in cases]
+    monkeypatch.setenv("FP8Q_GEMM_TILE_N", "128")
+    got = [c() for c in cases]
+    assert F.get_status() == F.OK
+    for i, (r, g) in enumerate(zip(ref, got)):
+        assert torch.equal(r, g), f"case {i}: 128-column tiles differ from 256-column tiles"
+    _full_check(got[0], qa, sa, qb, sb, "bf16")
+    _full_check(got[1], qx, sx, qd, sd, "f32", "1x128")
+
+
 # ------------------------------------------------- full-size workloads (bench sizes)
 def _sample_rows(M, n, seed):
     g = np.random.default_rng(seed)
