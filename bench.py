@@ -2,8 +2,8 @@
 """Benchmark of the block-scaled FP8 hot path on B300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload dense_fwd|square|dgrad|moe|moe_decode|moe_act_grad|
-                                wgrad|ksweep|quant]
+                    [--workload dense_fwd|square|dgrad|moe|moe_gather|moe_decode|
+                                moe_act_grad|wgrad|ksweep|quant]
                     [--legs device,e2e,cpu]
 
 Default workload (one "step" = the whole forward hot path of an FP8 Linear):
@@ -65,8 +65,8 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="dense_fwd",
-                    choices=["dense_fwd", "square", "dgrad", "moe", "moe_decode", "moe_act_grad",
-                             "wgrad", "ksweep", "quant"])
+                    choices=["dense_fwd", "square", "dgrad", "moe", "moe_gather", "moe_decode",
+                             "moe_act_grad", "wgrad", "ksweep", "quant"])
     ap.add_argument("--legs", default="device,e2e,cpu",
                     help="measurement legs to run: device (always), e2e, cpu")
     a = ap.parse_args(argv)
@@ -224,7 +224,7 @@ class DenseForward(Workload):
 class MoeGrouped(Workload):
     """quant_act(tokens, pow2) -> grouped GEMM over expert-sorted rows."""
 
-    def __init__(self, problem, device, decode=False):
+    def __init__(self, problem, device, decode=False, gather=False):
         import torch
         from fp8_block_scaled_17_b300 import fp8q as F
         self.F, self.torch, self.p = F, torch, problem
@@ -234,11 +234,15 @@ class MoeGrouped(Workload):
         self.qx = torch.empty((problem.tokens, K), dtype=torch.uint8, device=device)
         self.sx = torch.empty((K // 128, problem.tokens), dtype=torch.float32, device=device)
         F.quant_act_1x128(self.x, True, q=self.qx, sa=self.sx)
-        # dispatch (a row permutation to expert order), done once: the all-to-all
-        # that moves these rows between GPUs is not part of this single-GPU path
+        # dispatch (a row permutation to expert order): either done once here (the
+        # all-to-all that moves these rows between GPUs is not part of this
+        # single-GPU path), or fused into the GEMM as a row gather
         r = rows.to(device)
-        self.qa = self.qx.index_select(0, r).contiguous()
-        self.sa = self.sx.index_select(1, r).contiguous()
+        self.gather = gather
+        self.rows_i32 = r.to(torch.int32)
+        if not gather:
+            self.qa = self.qx.index_select(0, r).contiguous()
+            self.sa = self.sx.index_select(1, r).contiguous()
         self.offs = offs.to(device)
         self.qb = torch.empty((E, N, K), dtype=torch.uint8, device=device)
         self.sb = torch.empty((E, K // 128, N // 128), dtype=torch.float32, device=device)
@@ -246,6 +250,8 @@ class MoeGrouped(Workload):
             F.quant_w_128x128(w[e].to(device), q=self.qb[e], sb=self.sb[e])
         self.d = torch.empty((problem.rows, N), dtype=torch.bfloat16, device=device)
         self.name = getattr(self, "name", problem.name)
+        if gather:
+            self.name = problem.name + " (dispatch gather fused into the GEMM)"
         self.flops = problem.flops
         gemm = ("grouped_gemm", "tensor", problem.flops)
         if decode:  # weight-bandwidth bound: algorithmic bytes of codes, scales and D
@@ -261,6 +267,10 @@ class MoeGrouped(Workload):
 
     def calls(self):
         F = self.F
+        if self.gather:
+            return [lambda: F.quant_act_1x128(self.x, True, q=self.qx, sa=self.sx),
+                    lambda: F.grouped_gemm_gather(self.qx, self.sx, self.rows_i32, self.offs,
+                                                  self.qb, self.sb, d=self.d)]
         return [lambda: F.quant_act_1x128(self.x, True, q=self.qx, sa=self.sx),
                 lambda: F.grouped_gemm(self.qa, self.sa, self.offs, self.qb, self.sb, d=self.d)]
 
@@ -445,6 +455,8 @@ def make_workload(name, device):
         return Dgrad(W.DgradProblem(), device)
     if name == "moe":
         return MoeGrouped(W.MoeProblem(), device)
+    if name == "moe_gather":
+        return MoeGrouped(W.MoeProblem(), device, gather=True)
     if name == "moe_decode":
         return MoeGrouped(W.MOE_DECODE, device, decode=True)
     if name == "moe_act_grad":

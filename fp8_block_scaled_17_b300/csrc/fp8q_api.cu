@@ -150,7 +150,9 @@ bool env_flag(const char* name) {
   return v && v[0] && std::strcmp(v, "0") != 0;
 }
 
-fp8q_status gemm_common(const uint8_t* A, const float* sa, const int32_t* m_offsets, int E,
+// A is [a_rows][K]; without a row gather a_rows == M and row_index is null.
+fp8q_status gemm_common(const uint8_t* A, const float* sa, int64_t a_rows,
+                        const int32_t* row_index, const int32_t* m_offsets, int E,
                         const uint8_t* B, const float* sb, int64_t M, int64_t N, int64_t K,
                         void* D, int64_t ldd, unsigned flags, cudaStream_t stream) {
   using namespace fp8q::gemm;
@@ -162,10 +164,12 @@ fp8q_status gemm_common(const uint8_t* A, const float* sa, const int32_t* m_offs
   if (ldd < N) return FP8Q_ERR_SHAPE;
   if (E < 1 || E > kMaxExperts) return FP8Q_ERR_SHAPE;
   // TMA coordinates and tile counts are 32-bit
-  if (M >= (1ll << 31) || K >= (1ll << 31) || static_cast<int64_t>(E) * N >= (1ll << 31))
+  if (M >= (1ll << 31) || K >= (1ll << 31) || static_cast<int64_t>(E) * N >= (1ll << 31) ||
+      a_rows >= (1ll << 31))
     return FP8Q_ERR_SHAPE;
   if (M == 0) return FP8Q_OK;
   if (!A || !sa || !B || !sb || !D) return FP8Q_ERR_INVALID_ARG;
+  if (row_index && (a_rows <= 0 || !aligned4(row_index))) return FP8Q_ERR_INVALID_ARG;
   const int out_bytes = (flags & FP8Q_OUT_BF16) ? 2 : 4;
   if (!aligned16(A) || !aligned16(B) || !aligned16(D) || !aligned4(sa) || !aligned4(sb) ||
       (ldd * out_bytes) % 16)
@@ -179,11 +183,13 @@ fp8q_status gemm_common(const uint8_t* A, const float* sa, const int32_t* m_offs
   const int bn = (tn && std::strcmp(tn, "128") == 0) ? 128 : 256;
   if (bn == 128 ? !dev->gemm_ok : !dev->gemm256_ok) return FP8Q_ERR_UNSUPPORTED;
 
-  const uint32_t box_a_rows = static_cast<uint32_t>(M < BM ? M : BM);
+  // a gathered A tile is 32 tile::gather4 loads of four one-row boxes
+  const uint32_t box_a_rows = row_index ? 1u : static_cast<uint32_t>(M < BM ? M : BM);
+  const uint32_t a_tile_rows = row_index ? static_cast<uint32_t>(BM) : box_a_rows;
   const int64_t b_rows = static_cast<int64_t>(E) * N;
   const uint32_t box_b_rows = static_cast<uint32_t>(b_rows < bn ? b_rows : bn);
   CUtensorMap tmA, tmB;
-  if (!encode_u8_2d(&tmA, A, K, M, K, BK, box_a_rows)) return FP8Q_ERR_CUDA;
+  if (!encode_u8_2d(&tmA, A, K, a_rows, K, BK, box_a_rows)) return FP8Q_ERR_CUDA;
   if (!encode_u8_2d(&tmB, B, K, b_rows, K, BK, box_b_rows)) return FP8Q_ERR_CUDA;
 
   Params p;
@@ -191,6 +197,8 @@ fp8q_status gemm_common(const uint8_t* A, const float* sa, const int32_t* m_offs
   p.sb = sb;
   p.D = D;
   p.m_offsets = m_offsets;
+  p.row_index = row_index;
+  p.a_rows = a_rows;
   p.status = dev->status;
   p.M = M;
   p.ldd = ldd;
@@ -203,7 +211,7 @@ fp8q_status gemm_common(const uint8_t* A, const float* sa, const int32_t* m_offs
             ((reinterpret_cast<uintptr_t>(D) % 32 == 0 && (ldd * out_bytes) % 32 == 0) ? kFlagStore32
                                                                                    : 0);
   p.group_m = 16;
-  p.tx_bytes = (box_a_rows + box_b_rows) * BK;
+  p.tx_bytes = (a_tile_rows + box_b_rows) * BK;
   p.inject_timeout = env_flag("FP8Q_DEBUG_INJECT_TIMEOUT") ? 1 : 0;
   p.wait_limit_ns = kWaitLimitNs;
 
@@ -317,7 +325,7 @@ FP8Q_API fp8q_status fp8q_gemm_blockscaled(const uint8_t* A, const float* sa, co
                                            const float* sb, int64_t M, int64_t N, int64_t K,
                                            void* D, int64_t ldd, unsigned flags,
                                            fp8q_stream_t stream) {
-  return gemm_common(A, sa, nullptr, 1, B, sb, M, N, K, D, ldd, flags,
+  return gemm_common(A, sa, M, nullptr, nullptr, 1, B, sb, M, N, K, D, ldd, flags,
                      reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -326,7 +334,19 @@ FP8Q_API fp8q_status fp8q_grouped_gemm(const uint8_t* A, const float* sa,
                                        const float* sb, int64_t Mtot, int64_t N, int64_t K,
                                        void* D, unsigned flags, fp8q_stream_t stream) {
   if (!m_offsets) return FP8Q_ERR_INVALID_ARG;
-  return gemm_common(A, sa, m_offsets, E, B, sb, Mtot, N, K, D, N, flags,
+  return gemm_common(A, sa, Mtot, nullptr, m_offsets, E, B, sb, Mtot, N, K, D, N, flags,
+                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+FP8Q_API fp8q_status fp8q_grouped_gemm_gather(const uint8_t* A, const float* sa, int64_t T,
+                                              const int32_t* row_index,
+                                              const int32_t* m_offsets, int E,
+                                              const uint8_t* B, const float* sb, int64_t Mtot,
+                                              int64_t N, int64_t K, void* D, unsigned flags,
+                                              fp8q_stream_t stream) {
+  if (!m_offsets || !row_index) return FP8Q_ERR_INVALID_ARG;
+  if (T < 0) return FP8Q_ERR_SHAPE;
+  return gemm_common(A, sa, T, row_index, m_offsets, E, B, sb, Mtot, N, K, D, N, flags,
                      reinterpret_cast<cudaStream_t>(stream));
 }
 

@@ -19,7 +19,9 @@
 //              and BN/2 FP32 accumulators in registers. Per chunk it loads P_kb
 //              from TMEM and does acc += P_kb * (sa[kb][m] * sb[kb][n/128]).
 //   warp 8     TMA producer: A (128 x 128 B) and B (BN x 128 B) tiles into a
-//              shared-memory ring, 128-byte swizzled.
+//              shared-memory ring, 128-byte swizzled. With a row gather (the
+//              MoE dispatch fused into the grouped GEMM) every lane loads four
+//              A rows of the tile by index with one tile::gather4 TMA load.
 //   warp 9     TMEM allocator + MMA issuer (one thread).
 //   warp 10    scale loader: copies (cp.async) the scales of each chunk into a
 //              shared-memory ring: sa of the tile's 128 rows and the B scales
@@ -48,7 +50,7 @@ namespace fp8q {
 
 // Error bits recorded by kernels (read and cleared by fp8q_get_status).
 constexpr unsigned kDevStatusTimeout = 1u;
-constexpr unsigned kDevStatusBadOffsets = 2u;
+constexpr unsigned kDevStatusBadOffsets = 2u;  // also: gather indices out of range
 
 namespace gemm {
 
@@ -102,10 +104,12 @@ struct Cfg {
 };
 
 struct Params {
-  const float* sa;            // [K/128][M]
+  const float* sa;            // [K/128][a_rows]
   const float* sb;            // [E][K/128][N/128] or, 1x128 mode, [K/128][N]
   void* D;                    // [M][ldd]
   const int32_t* m_offsets;   // [E+1] (device) or null for a dense GEMM
+  const int32_t* row_index;   // [M] (device): A row of each output row, or null
+  int64_t a_rows;             // rows of A (and columns of sa): M without a gather
   unsigned* status;           // device status word
   int64_t M;                  // rows of A (Mtot)
   int64_t ldd;
@@ -151,6 +155,28 @@ __device__ __forceinline__ Tile tile_at(int t, const int* seg, const int* pre, i
   tl.n0 = (r / gs) * bn;
   tl.brow0 = e * N + tl.n0;
   return tl;
+}
+
+// Row of A that output row m of tile tl reads: row m itself, or row_index[m]
+// with a gather. Rows past the tile's segment read row 0 (their outputs are
+// masked); an index outside [0, a_rows) is clamped and reported.
+__device__ __forceinline__ int64_t a_row(const Params& p, const Tile& tl, int64_t m) {
+  if (!p.row_index) return m;
+  if (m >= tl.m_end) return 0;
+  const int64_t r = __ldg(p.row_index + m);
+  if (r < 0 || r >= p.a_rows) {
+    atomicOr(p.status, kDevStatusBadOffsets);
+    return r < 0 ? 0 : p.a_rows - 1;
+  }
+  return r;
+}
+
+// The same row without the report (the producer warp reports bad indices).
+__device__ __forceinline__ int32_t a_row_quiet(const Params& p, const Tile& tl, int64_t m) {
+  if (!p.row_index) return static_cast<int32_t>(m);
+  if (m >= tl.m_end) return 0;
+  const int32_t r = __ldg(p.row_index + m);
+  return r < 0 ? 0 : (r >= p.a_rows ? static_cast<int32_t>(p.a_rows - 1) : r);
 }
 
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
@@ -309,7 +335,52 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp >= kPromoWarps) {
     if constexpr (C::kSplitRegs) setmaxnreg_dec<kCtrlRegs>();
-    if (warp == kProducerWarp) {
+    if (warp == kProducerWarp && p.row_index) {
+      // ---------------------------------------- TMA producer, gathered rows
+      // Lane l loads rows 4l .. 4l+3 of the A tile (one gather4 box of 128
+      // bytes each) into rows 4l .. of the stage; lane 0 also loads B and owns
+      // the barrier traffic.
+      int stage = 0;
+      uint32_t phase = 0;
+      int issued = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        const Tile tl = tile_at(t, seg, pre, p.E, nt, p.N, p.group_m, BN);
+        const int64_t r0 = tl.m0 + 4 * lane;
+        const int32_t g0 = static_cast<int32_t>(a_row(p, tl, r0));
+        const int32_t g1 = static_cast<int32_t>(a_row(p, tl, r0 + 1));
+        const int32_t g2 = static_cast<int32_t>(a_row(p, tl, r0 + 2));
+        const int32_t g3 = static_cast<int32_t>(a_row(p, tl, r0 + 3));
+        for (int kb = 0; kb < KB; ++kb) {
+          bool w = true;
+          if (lane == 0) {
+            w = wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, p, p.wait_limit_ns);
+            if (w) mbar_arrive_expect_tx(full_bar(stage), p.tx_bytes);
+          }
+          if (!__shfl_sync(0xffffffffu, w, 0)) {
+            ok = false;
+            break;
+          }
+          tma_gather4_2d(base + C::a_off + stage * kABytes + 512u * lane, &tmA, full_bar(stage),
+                         kb * BK, g0, g1, g2, g3);
+          if (lane == 0)
+            tma_load_2d(base + C::b_off + stage * C::kBBytes, &tmB, full_bar(stage), kb * BK,
+                        tl.brow0);
+          ++issued;
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        }
+      }
+      if (!ok && lane == 0) {  // let the loads still in flight land before the CTA exits
+        const int n = issued < kStages ? issued : kStages;
+        for (int i = 1; i <= n; ++i) {
+          int s = stage - i;
+          uint32_t ph = phase;
+          if (s < 0) { s += kStages; ph ^= 1u; }
+          wait_drain(full_bar(s), ph, p.wait_limit_ns);
+        }
+      }
+      __syncwarp();
+    } else if (warp == kProducerWarp) {
       // ----------------------------------------------------- TMA producer
       if (lane == 0) {
         int stage = 0;
@@ -410,11 +481,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int64_t left = tl.m_end - tl.m0;
         const int rows = left < BM ? static_cast<int>(left) : BM;
         const int cols = p.N - tl.n0;  // columns of B in this tile (BN or fewer)
-        const float* sa_src = p.sa + tl.m0 + lane;
+        // sa of this lane's rows m0 + lane + 32 i (gathered rows: sa of their A
+        // row), at sa_kb + ar[i] for the current K-block's row sa_kb of sa
+        int32_t ar[BM / 32];
+#pragma unroll
+        for (int i = 0; i < BM / 32; ++i)
+          ar[i] = a_row_quiet(p, tl, tl.m0 + lane + 32 * i);
+        const float* sa_kb = p.sa;
         // B scales of this lane (block mode: lanes < BN/128; 1x128 mode: 4 columns x BN/128)
         const float* sb_src = sb1 ? p.sb + tl.n0 + 4 * lane
                                   : p.sb + static_cast<int64_t>(tl.e) * KB * NB + tl.n0 / 128 + lane;
-        const int64_t sa_step = promote ? p.M : 0;
+        const int64_t sa_step = promote ? p.a_rows : 0;
         const int64_t sb_step = promote ? (sb1 ? p.N : NB) : 0;
         for (int u = 0; u < units; ++u) {
           if (sub == 0 &&
@@ -426,7 +503,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int i = 0; i < BM / 32; ++i) {
             const bool in = 32 * i + lane < rows;
-            cp_async_4(dst + 128u * i, in ? sa_src + 32 * i : p.sa, in ? 4u : 0u);
+            cp_async_4(dst + 128u * i, in ? sa_kb + ar[i] : p.sa, in ? 4u : 0u);
           }
           if (!sb1) {
             if (lane < BN / 128) {
@@ -441,7 +518,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                           in ? 16u : 0u);
             }
           }
-          sa_src += sa_step;
+          sa_kb += sa_step;
           sb_src += sb_step;
           if (++sub == group_u) {
             cp_async_mbar_arrive_noinc(sfull_bar(slot));

@@ -68,6 +68,19 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// Four rows y0..y3 of a 2D tensor, one box (one row high) each, columns x.. ,
+// into consecutive rows of shared memory at dst (row gather); completion is
+// signalled on `bar` as transaction bytes.
+__device__ __forceinline__ void tma_gather4_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                               int32_t x, int32_t y0, int32_t y1, int32_t y2,
+                                               int32_t y3) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3)
+      : "memory");
+}
+
 // --------------------------------------------------------------- cp.async
 // 4-byte copy global -> shared; src_bytes = 0 writes zeros and reads nothing.
 __device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src, uint32_t src_bytes) {

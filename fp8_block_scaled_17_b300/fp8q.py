@@ -26,7 +26,8 @@ OUT_BF16 = 16
 W_KN_LAYOUT = 32
 
 EXPORTED = ("fp8q_quant_act_1x128", "fp8q_quant_w_128x128", "fp8q_requant_1x128_to_128x1",
-            "fp8q_gemm_blockscaled", "fp8q_grouped_gemm", "fp8q_get_status",
+            "fp8q_gemm_blockscaled", "fp8q_grouped_gemm", "fp8q_grouped_gemm_gather",
+            "fp8q_get_status",
             "fp8q_status_string")
 
 
@@ -48,6 +49,8 @@ def _load() -> ctypes.CDLL:
         "fp8q_requant_1x128_to_128x1": [vp, vp, i64, i64, vp, vp, u32, vp],
         "fp8q_gemm_blockscaled": [vp, vp, vp, vp, i64, i64, i64, vp, i64, u32, vp],
         "fp8q_grouped_gemm": [vp, vp, vp, i32, vp, vp, i64, i64, i64, vp, u32, vp],
+        "fp8q_grouped_gemm_gather": [vp, vp, i64, vp, vp, i32, vp, vp, i64, i64, i64, vp, u32,
+                                     vp],
         "fp8q_get_status": [vp],
         "fp8q_status_string": [i32],
     }
@@ -171,4 +174,27 @@ def grouped_gemm(a: torch.Tensor, sa: torch.Tensor, m_offsets: torch.Tensor, b: 
     flags = (OUT_BF16 if d.dtype == torch.bfloat16 else 0) | (NO_PROMOTION if no_promotion else 0)
     _check(LIB.fp8q_grouped_gemm(_ptr(a), _ptr(sa), _ptr(m_offsets), E, _ptr(b), _ptr(sb), Mtot,
                                  N, K, _ptr(d), flags, _stream(stream)), "fp8q_grouped_gemm")
+    return d
+
+
+def grouped_gemm_gather(a: torch.Tensor, sa: torch.Tensor, row_index: torch.Tensor,
+                        m_offsets: torch.Tensor, b: torch.Tensor, sb: torch.Tensor,
+                        out_dtype=torch.bfloat16, no_promotion: bool = False,
+                        d: torch.Tensor | None = None, stream=None):
+    """token-order codes a [T][K], sa [K/128][T]; row_index int32 [Mtot] (device):
+    the token of each expert-ordered row; m_offsets int32 [E+1] (device);
+    b [E][N][K], sb [E][K/128][N/128] -> D [Mtot][N] in expert order."""
+    assert m_offsets.dtype == torch.int32 and m_offsets.is_cuda
+    assert row_index.dtype == torch.int32 and row_index.is_cuda and row_index.is_contiguous()
+    assert a.is_contiguous() and b.is_contiguous() and sa.is_contiguous() and sb.is_contiguous()
+    T, K = a.shape
+    E, N, _ = b.shape
+    Mtot = row_index.numel()
+    if d is None:
+        d = torch.empty((Mtot, N), dtype=out_dtype, device=a.device)
+    assert d.is_contiguous()
+    flags = (OUT_BF16 if d.dtype == torch.bfloat16 else 0) | (NO_PROMOTION if no_promotion else 0)
+    _check(LIB.fp8q_grouped_gemm_gather(_ptr(a), _ptr(sa), T, _ptr(row_index), _ptr(m_offsets),
+                                        E, _ptr(b), _ptr(sb), Mtot, N, K, _ptr(d), flags,
+                                        _stream(stream)), "fp8q_grouped_gemm_gather")
     return d

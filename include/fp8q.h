@@ -161,10 +161,29 @@ fp8q_status fp8q_grouped_gemm(const uint8_t* A, const float* sa, const int32_t* 
                               int64_t K, void* D, unsigned flags, fp8q_stream_t stream);
 
 /*
+ * The grouped GEMM with the MoE dispatch fused in [HEARAON, paragraph on
+ * quantizing the activation to FP8 before the MoE up-projection and then
+ * applying the dispatch]: the tokens are quantized once, in token order, and
+ * row r of the expert-ordered problem reads token row_index[r] directly (TMA
+ * row gather), so no expert-ordered copy of A or sa is made. Same arithmetic
+ * and output as fp8q_grouped_gemm on the gathered rows, bit for bit.
+ * A         : uint8 codes [T][K] (token order), sa float32 [K/128][T].
+ * row_index : DEVICE int32 [Mtot], each in [0, T); indices outside are clamped
+ *             and reported by fp8q_get_status as FP8Q_ERR_INVALID_ARG.
+ * m_offsets, B, sb, D, flags: as fp8q_grouped_gemm (D in expert order).
+ * T > 0 when Mtot > 0; row_index 4-byte aligned.
+ */
+fp8q_status fp8q_grouped_gemm_gather(const uint8_t* A, const float* sa, int64_t T,
+                                     const int32_t* row_index, const int32_t* m_offsets, int E,
+                                     const uint8_t* B, const float* sb, int64_t Mtot, int64_t N,
+                                     int64_t K, void* D, unsigned flags, fp8q_stream_t stream);
+
+/*
  * Synchronizes `stream`, then reports (and clears) errors that kernels of the
  * current device recorded: FP8Q_ERR_TIMEOUT if a pipeline wait exceeded its
  * limit (the kernel stopped early: its outputs are invalid, the context stays
- * usable), FP8Q_ERR_INVALID_ARG for malformed grouped-GEMM offsets,
+ * usable), FP8Q_ERR_INVALID_ARG for malformed grouped-GEMM offsets or gather
+ * indices,
  * FP8Q_ERR_CUDA if the stream reported a CUDA error. No counterpart in the
  * pages: this is the library's failure-detection hook.
  * Tuning: FP8Q_GEMM_TILE_N=128 selects 128x128 CTA tiles (four TMEM
