@@ -2,8 +2,8 @@
 """Benchmark of the block-scaled FP8 hot path on B300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload dense_fwd|square|dgrad|moe|moe_gather|moe_decode|
-                                moe_act_grad|wgrad|ksweep|quant]
+                    [--workload dense_fwd|square|dgrad|moe|moe_scatter|moe_gather|
+                                moe_decode|moe_act_grad|wgrad|ksweep|quant]
                     [--legs device,e2e,cpu]
 
 Default workload (one "step" = the whole forward hot path of an FP8 Linear):
@@ -65,8 +65,8 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="dense_fwd",
-                    choices=["dense_fwd", "square", "dgrad", "moe", "moe_gather", "moe_decode",
-                             "moe_act_grad", "wgrad", "ksweep", "quant"])
+                    choices=["dense_fwd", "square", "dgrad", "moe", "moe_scatter", "moe_gather",
+                             "moe_decode", "moe_act_grad", "wgrad", "ksweep", "quant"])
     ap.add_argument("--legs", default="device,e2e,cpu",
                     help="measurement legs to run: device (always), e2e, cpu")
     a = ap.parse_args(argv)
@@ -224,9 +224,10 @@ class DenseForward(Workload):
 class MoeGrouped(Workload):
     """quant_act(tokens, pow2) -> grouped GEMM over expert-sorted rows."""
 
-    def __init__(self, problem, device, decode=False, gather=False):
+    def __init__(self, problem, device, decode=False, gather=False, scatter=False):
         import torch
         from fp8_block_scaled_17_b300 import fp8q as F
+        from fp8_block_scaled_17_b300 import workloads as W
         self.F, self.torch, self.p = F, torch, problem
         x, w, rows, offs = problem.make()
         self.x = x.to(device)
@@ -238,8 +239,9 @@ class MoeGrouped(Workload):
         # all-to-all that moves these rows between GPUs is not part of this
         # single-GPU path), or fused into the GEMM as a row gather
         r = rows.to(device)
-        self.gather = gather
+        self.gather, self.scatter = gather, scatter
         self.rows_i32 = r.to(torch.int32)
+        self.dest = W.dispatch_destinations(rows, problem.tokens, problem.topk).to(device)
         if not gather:
             self.qa = self.qx.index_select(0, r).contiguous()
             self.sa = self.sx.index_select(1, r).contiguous()
@@ -252,6 +254,8 @@ class MoeGrouped(Workload):
         self.name = getattr(self, "name", problem.name)
         if gather:
             self.name = problem.name + " (dispatch gather fused into the GEMM)"
+        if scatter:
+            self.name = problem.name + " (dispatch fused into the quantizer)"
         self.flops = problem.flops
         gemm = ("grouped_gemm", "tensor", problem.flops)
         if decode:  # weight-bandwidth bound: algorithmic bytes of codes, scales and D
@@ -261,12 +265,19 @@ class MoeGrouped(Workload):
             self.name = problem.name + " (decode: few rows per expert, weight-bandwidth bound)"
         self.kernels = [("quant_act_1x128_pow2", "hbm", problem.tokens * K * (2 + 1 + 4 / 128)),
                         gemm]
+        if scatter:  # reads the tokens once, writes every routed copy
+            self.kernels[0] = ("quant_act_1x128_scatter_pow2", "hbm",
+                               problem.tokens * K * 2 + problem.rows * K * (1 + 4 / 128))
         self.config = {"tokens": problem.tokens, "experts": E, "topk": problem.topk,
                        "rows": problem.rows, "K": K, "N": N,
                        "expert_rows": (offs[1:] - offs[:-1]).tolist(), "out": "bf16"}
 
     def calls(self):
         F = self.F
+        if self.scatter:
+            return [lambda: F.quant_act_1x128_scatter(self.x, self.dest, self.p.rows, True,
+                                                      q=self.qa, sa=self.sa),
+                    lambda: F.grouped_gemm(self.qa, self.sa, self.offs, self.qb, self.sb, d=self.d)]
         if self.gather:
             return [lambda: F.quant_act_1x128(self.x, True, q=self.qx, sa=self.sx),
                     lambda: F.grouped_gemm_gather(self.qx, self.sx, self.rows_i32, self.offs,
@@ -455,6 +466,8 @@ def make_workload(name, device):
         return Dgrad(W.DgradProblem(), device)
     if name == "moe":
         return MoeGrouped(W.MoeProblem(), device)
+    if name == "moe_scatter":
+        return MoeGrouped(W.MoeProblem(), device, scatter=True)
     if name == "moe_gather":
         return MoeGrouped(W.MoeProblem(), device, gather=True)
     if name == "moe_decode":

@@ -86,8 +86,10 @@ fp8q_status device_info(DeviceInfo** out) {
       using namespace fp8q;
       const int rs = kRowSmemBytes, cs0 = col_smem_bytes<0>(), cs1 = col_smem_bytes<1>();
       d.occ_rows = d.occ_cols_bf16 = d.occ_cols_codes = d.occ_blocks = 1;
-      if (!setup_quant_kernel(quant_rows_1x128_kernel<false>, rs, &d.occ_rows) ||
-          !setup_quant_kernel(quant_rows_1x128_kernel<true>, rs, &d.occ_rows) ||
+      if (!setup_quant_kernel(quant_rows_1x128_kernel<false, false>, rs, &d.occ_rows) ||
+          !setup_quant_kernel(quant_rows_1x128_kernel<true, false>, rs, &d.occ_rows) ||
+          !setup_quant_kernel(quant_rows_1x128_kernel<false, true>, rs, &d.occ_rows) ||
+          !setup_quant_kernel(quant_rows_1x128_kernel<true, true>, rs, &d.occ_rows) ||
           !setup_quant_kernel(quant_cols_kernel<0, false, false>, cs0, &d.occ_cols_bf16) ||
           !setup_quant_kernel(quant_cols_kernel<0, false, true>, cs0, &d.occ_cols_bf16) ||
           !setup_quant_kernel(quant_cols_kernel<0, true, false>, cs0, &d.occ_cols_bf16) ||
@@ -254,9 +256,11 @@ FP8Q_API fp8q_status fp8q_quant_act_1x128(const void* x, int64_t M, int64_t K, i
     const unsigned grid = persistent_grid(units, dev->num_sms, dev->occ_rows);
     const int smem = fp8q::kRowSmemBytes;
     if (pow2)
-      fp8q::quant_rows_1x128_kernel<true><<<grid, 256, smem, s>>>(xb, M, KB, ldx, q, ldq, sa);
+      fp8q::quant_rows_1x128_kernel<true, false>
+          <<<grid, 256, smem, s>>>(xb, M, KB, ldx, q, ldq, sa, nullptr, 0, M);
     else
-      fp8q::quant_rows_1x128_kernel<false><<<grid, 256, smem, s>>>(xb, M, KB, ldx, q, ldq, sa);
+      fp8q::quant_rows_1x128_kernel<false, false>
+          <<<grid, 256, smem, s>>>(xb, M, KB, ldx, q, ldq, sa, nullptr, 0, M);
   } else {
     // stored [K][M]: R = K rows, Cc = M columns, 128x1 column tiles
     const int64_t tiles = ((M + 127) / 128) * (K / 128);
@@ -267,6 +271,37 @@ FP8Q_API fp8q_status fp8q_quant_act_1x128(const void* x, int64_t M, int64_t K, i
     else
       fp8q::quant_cols_kernel<0, false, false><<<grid, 256, smem, s>>>(x, K, M, ldx, nullptr, q, ldq, sa);
   }
+  return launch_status();
+}
+
+FP8Q_API fp8q_status fp8q_quant_act_1x128_scatter(const void* x, int64_t T, int64_t K,
+                                                  int64_t ldx, const int32_t* dest, int topk,
+                                                  uint8_t* q, int64_t ldq, float* sa,
+                                                  int64_t Mtot, unsigned flags,
+                                                  fp8q_stream_t stream) {
+  if (flags & ~static_cast<unsigned>(FP8Q_POW2_SCALE)) return FP8Q_ERR_INVALID_ARG;
+  if (T < 0 || K <= 0 || K % 128 || topk < 1 || Mtot < 0) return FP8Q_ERR_SHAPE;
+  if (ldq < K || ldx < K) return FP8Q_ERR_SHAPE;
+  if (K / 128 >= (1ll << 31) || T >= (1ll << 40) || Mtot >= (1ll << 40)) return FP8Q_ERR_SHAPE;
+  if (T == 0 || Mtot == 0) return FP8Q_OK;
+  if (!x || !dest || !q || !sa) return FP8Q_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(q) || !aligned4(sa) || !aligned4(dest) || (ldx * 2) % 16 ||
+      ldq % 16)
+    return FP8Q_ERR_ALIGN;
+  DeviceInfo* dev = nullptr;
+  if (fp8q_status st = device_info(&dev)) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const auto* xb = static_cast<const __nv_bfloat16*>(x);
+  const int KB = static_cast<int>(K / 128);
+  const int64_t units = ((T + fp8q::kRowUnitRows - 1) / fp8q::kRowUnitRows) * KB;
+  const unsigned grid = persistent_grid(units, dev->num_sms, dev->occ_rows);
+  const int smem = fp8q::kRowSmemBytes;
+  if (flags & FP8Q_POW2_SCALE)
+    fp8q::quant_rows_1x128_kernel<true, true>
+        <<<grid, 256, smem, s>>>(xb, T, KB, ldx, q, ldq, sa, dest, topk, Mtot);
+  else
+    fp8q::quant_rows_1x128_kernel<false, true>
+        <<<grid, 256, smem, s>>>(xb, T, KB, ldx, q, ldq, sa, dest, topk, Mtot);
   return launch_status();
 }
 

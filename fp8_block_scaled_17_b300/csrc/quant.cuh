@@ -144,10 +144,14 @@ constexpr int kRowUnitRows = 64;
 constexpr int kRowStages = 4;
 constexpr int kRowSmemBytes = kRowStages * kRowUnitRows * 256;  // 64 KB
 
-template <bool kPow2>
+// kScatter: the MoE dispatch fused in. Row r of x is quantized once and its
+// codes and scale are written to rows dest[r * topk + j] (j < topk) of q and sa
+// (q has Mq rows, sa is [KB][Mq]); a destination outside [0, Mq) is skipped.
+template <bool kPow2, bool kScatter>
 __global__ void __launch_bounds__(256) quant_rows_1x128_kernel(
     const __nv_bfloat16* __restrict__ x, int64_t M, int KB, int64_t ldx,
-    uint8_t* __restrict__ q, int64_t ldq, float* __restrict__ sa) {
+    uint8_t* __restrict__ q, int64_t ldq, float* __restrict__ sa,
+    const int32_t* __restrict__ dest, int topk, int64_t Mq) {
   extern __shared__ __align__(16) uint8_t smem[];
   const int hw = threadIdx.x >> 4;
   const int l = threadIdx.x & 15;
@@ -224,8 +228,18 @@ __global__ void __launch_bounds__(256) quant_rows_1x128_kernel(
       out.x = quant4(ts, f[0], f[1], f[2], f[3]);
       out.y = quant4(ts, f[4], f[5], f[6], f[7]);
       if (r < M) {
-        *reinterpret_cast<uint2*>(q + r * ldq + kb * 128 + l * 8) = out;
-        if (l == 0) sa[static_cast<int64_t>(kb) * M + r] = ts.s;
+        if (!kScatter) {
+          *reinterpret_cast<uint2*>(q + r * ldq + kb * 128 + l * 8) = out;
+          if (l == 0) sa[static_cast<int64_t>(kb) * M + r] = ts.s;
+        } else {
+          for (int j = 0; j < topk; ++j) {
+            const int64_t d = __ldg(dest + r * topk + j);
+            if (d >= 0 && d < Mq) {
+              *reinterpret_cast<uint2*>(q + d * ldq + kb * 128 + l * 8) = out;
+              if (l == 0) sa[static_cast<int64_t>(kb) * Mq + d] = ts.s;
+            }
+          }
+        }
       }
     }
     advance(cur);

@@ -25,7 +25,7 @@ NO_PROMOTION = 8
 OUT_BF16 = 16
 W_KN_LAYOUT = 32
 
-EXPORTED = ("fp8q_quant_act_1x128", "fp8q_quant_w_128x128", "fp8q_requant_1x128_to_128x1",
+EXPORTED = ("fp8q_quant_act_1x128", "fp8q_quant_act_1x128_scatter", "fp8q_quant_w_128x128", "fp8q_requant_1x128_to_128x1",
             "fp8q_gemm_blockscaled", "fp8q_grouped_gemm", "fp8q_grouped_gemm_gather",
             "fp8q_get_status",
             "fp8q_status_string")
@@ -45,6 +45,7 @@ def _load() -> ctypes.CDLL:
     vp, i64, u32, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_uint, ctypes.c_int
     sig = {
         "fp8q_quant_act_1x128": [vp, i64, i64, i64, vp, i64, vp, u32, vp],
+        "fp8q_quant_act_1x128_scatter": [vp, i64, i64, i64, vp, i32, vp, i64, vp, i64, u32, vp],
         "fp8q_quant_w_128x128": [vp, i64, i64, vp, vp, u32, vp],
         "fp8q_requant_1x128_to_128x1": [vp, vp, i64, i64, vp, vp, u32, vp],
         "fp8q_gemm_blockscaled": [vp, vp, vp, vp, i64, i64, i64, vp, i64, u32, vp],
@@ -104,6 +105,27 @@ def quant_act_1x128(x: torch.Tensor, pow2: bool = False, transposed_input: bool 
     flags = (POW2_SCALE if pow2 else 0) | (TRANSPOSED_INPUT if transposed_input else 0)
     _check(LIB.fp8q_quant_act_1x128(_ptr(x), M, K, x.stride(0), _ptr(q), q.stride(0), _ptr(sa),
                                     flags, _stream(stream)), "fp8q_quant_act_1x128")
+    return q, sa
+
+
+def quant_act_1x128_scatter(x: torch.Tensor, dest: torch.Tensor, Mtot: int, pow2: bool = False,
+                            q: torch.Tensor | None = None, sa: torch.Tensor | None = None,
+                            stream=None):
+    """x bf16 [T][K], dest int32 [T][topk] (device): expert-ordered rows of each
+    token -> (codes u8 [Mtot][K], scales f32 [K/128][Mtot]); the MoE dispatch
+    fused into the quantization."""
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
+    assert dest.dtype == torch.int32 and dest.is_cuda and dest.dim() == 2 and dest.is_contiguous()
+    T, K = x.shape
+    assert dest.shape[0] == T
+    if q is None:
+        q = torch.empty((Mtot, K), dtype=torch.uint8, device=x.device)
+    if sa is None:
+        sa = torch.empty((K // 128, Mtot), dtype=torch.float32, device=x.device)
+    _check(LIB.fp8q_quant_act_1x128_scatter(_ptr(x), T, K, x.stride(0), _ptr(dest),
+                                            dest.shape[1], _ptr(q), q.stride(0), _ptr(sa), Mtot,
+                                            POW2_SCALE if pow2 else 0, _stream(stream)),
+           "fp8q_quant_act_1x128_scatter")
     return q, sa
 
 

@@ -50,6 +50,14 @@ def moe_routing(tokens: int, experts: int, topk: int, zipf: float = 1.1, seed: i
     return tok[order], offs.to(torch.int32)
 
 
+def dispatch_destinations(rows: torch.Tensor, tokens: int, topk: int) -> torch.Tensor:
+    """The inverse of the routing permutation: dest[t][j] is the expert-ordered
+    row of token t's j-th copy (rows lists the token of each expert-ordered row;
+    every token appears exactly topk times)."""
+    order = torch.argsort(rows, stable=True)
+    return order.to(torch.int32).view(tokens, topk)
+
+
 @dataclass
 class GemmProblem:
     """Logical problem: D[M][N] = A[M][K] . W[K][N] (A row-major, W input-major)."""

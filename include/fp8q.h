@@ -88,6 +88,26 @@ fp8q_status fp8q_quant_act_1x128(const void* x, int64_t M, int64_t K, int64_t ld
                                  fp8q_stream_t stream);
 
 /*
+ * 1x128 activation quantization with the MoE dispatch fused in [HEARAON,
+ * paragraph on quantizing the activation to FP8 before the MoE up-projection
+ * and then applying the dispatch]: token row t of x is quantized once and its
+ * codes and scales are written to the expert-ordered rows dest[t*topk + j],
+ * j < topk, of q and sa, which then feed fp8q_grouped_gemm directly.
+ * x    : bf16 [T][K], row stride ldx elements (ldx >= K).
+ * dest : DEVICE int32 [T][topk]; a destination outside [0, Mtot) is skipped.
+ * q    : uint8 codes [Mtot][K], row stride ldq bytes (ldq >= K).
+ * sa   : float32 [K/128][Mtot].
+ * T >= 0, Mtot >= 0 (either 0 is a no-op), K > 0 and K % 128 == 0, topk >= 1.
+ * x and q 16-byte aligned (rows included); sa and dest 4-byte aligned.
+ * flags: FP8Q_POW2_SCALE. Codes and scales equal those of fp8q_quant_act_1x128
+ * on the gathered rows, bit for bit.
+ */
+fp8q_status fp8q_quant_act_1x128_scatter(const void* x, int64_t T, int64_t K, int64_t ldx,
+                                         const int32_t* dest, int topk, uint8_t* q,
+                                         int64_t ldq, float* sa, int64_t Mtot, unsigned flags,
+                                         fp8q_stream_t stream);
+
+/*
  * 128x128 weight-block quantization [WHY-BE].
  * w  : bf16 [K][N] row-major (input channels x output channels), contiguous.
  * q  : uint8 codes [N][K] (transposed: K-major, the GEMM's B operand for the

@@ -161,3 +161,17 @@ def test_moe_gather_full_matches_pregathered(F):
                          sx.index_select(1, ri.long()).contiguous(), od, qb, sb)
     assert F.get_status() == F.OK
     assert torch.equal(d, ref)
+
+
+def test_moe_scatter_full_matches_gather(F):
+    """The bench's MoE workload with the dispatch fused into the quantizer: the
+    expert-ordered codes and scales equal the gathered quantization, bit for bit."""
+    p = W.MoeProblem()
+    x, _, rows, _ = p.make()
+    xd = x.cuda()
+    qx, sx = F.quant_act_1x128(xd, True)
+    r = rows.cuda()
+    dest = W.dispatch_destinations(rows, p.tokens, p.topk).cuda()
+    qa, sa = F.quant_act_1x128_scatter(xd, dest, p.rows, True)
+    assert torch.equal(qa, qx.index_select(0, r))
+    assert torch.equal(sa, sx.index_select(1, r))

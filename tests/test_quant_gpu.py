@@ -105,6 +105,35 @@ def test_quant_w_kn_layout(F, K, N, pow2):
     _assert_same(q, sb, np.ascontiguousarray(rq.T), np.ascontiguousarray(rs.T))
 
 
+@pytest.mark.parametrize("T,K,E,topk,pow2", [(300, 384, 4, 2, True), (65, 256, 3, 3, False),
+                                             (1000, 512, 8, 3, True)])
+def test_quant_act_scatter(F, T, K, E, topk, pow2):
+    """The MoE dispatch fused into the 1x128 quantizer: codes and scales written to
+    the expert-ordered rows equal the quantization of the gathered rows, bit for
+    bit (and the oracle's)."""
+    x = W.bf16_normal((T, K), 1.0, seed=T + K, outlier_frac=0.002, outlier_scale=30.0)
+    rows, _ = W.moe_routing(T, E, topk, seed=T)
+    dest = W.dispatch_destinations(rows, T, topk).cuda()
+    q, sa = F.quant_act_1x128_scatter(x.cuda(), dest, rows.numel(), pow2)
+    _assert_same(q, sa, *O.quant_act_1x128(x[rows].float().numpy(), pow2))
+
+
+def test_quant_act_scatter_skips_invalid_destinations(F):
+    T, K = 130, 256
+    x = W.bf16_normal((T, K), 1.0, seed=9).cuda()
+    dest = torch.arange(2 * T, dtype=torch.int32, device="cuda").view(T, 2)
+    dest[5, 1] = -1
+    dest[7, 0] = 2 * T + 3
+    q = torch.full((2 * T, K), 0xAB, dtype=torch.uint8, device="cuda")
+    sa = torch.full((K // 128, 2 * T), -1.0, dtype=torch.float32, device="cuda")
+    F.quant_act_1x128_scatter(x, dest, 2 * T, q=q, sa=sa)
+    ref_q, ref_s = F.quant_act_1x128(x)
+    assert (q[11] == 0xAB).all() and (sa[:, 11] == -1).all()   # row 5's skipped copy
+    assert (q[14] == 0xAB).all() and (sa[:, 14] == -1).all()   # row 7's out-of-range copy
+    assert torch.equal(q[10], ref_q[5]) and torch.equal(q[15], ref_q[7])
+    assert torch.equal(sa[:, 10], ref_s[:, 5])
+
+
 # ----------------------------------------------------------- requant 1x128 -> 128x1
 @pytest.mark.parametrize("T,C,pow2", [(256, 384, True), (384, 256, False), (128, 128, True)])
 def test_requant(F, T, C, pow2):

@@ -24,3 +24,13 @@ def test_moe_routing_structure():
         assert (seg[1:] > seg[:-1]).all()
     sizes = (offs[1:] - offs[:-1]).float()
     assert sizes[0] > sizes[-1]  # Zipf: the most popular expert gets the most rows
+
+
+def test_dispatch_destinations_invert_the_routing():
+    rows, offs = W.moe_routing(tokens=200, experts=8, topk=3, seed=4)
+    dest = W.dispatch_destinations(rows, 200, 3)
+    assert dest.shape == (200, 3)
+    flat = dest.flatten().long()
+    assert torch.equal(torch.sort(flat).values, torch.arange(600))   # a permutation
+    for t in (0, 57, 199):
+        assert (rows[dest[t].long()] == t).all()                      # each lands on token t
