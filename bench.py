@@ -599,6 +599,9 @@ def run_ours(args):
     wl = make_workload(args.workload, device)
     peaks = load_peaks()
     fp8_peak = 2.0 * peaks["bf16_tflops"]
+    # nominal dense FP8 rate: 16384 flop per clock per SM at the 2032 MHz maximum clock
+    fp8_nominal = (torch.cuda.get_device_properties(device).multi_processor_count
+                   * 16384 * 2.032e9 / 1e12)
     calls = wl.calls()
     pre = wl.pre
 
@@ -670,7 +673,7 @@ def run_ours(args):
         else:
             tf = units / (ms / 1e3) / 1e12
             entry.update({"TFLOP/s": round(tf, 1), "frac_fp8": round(tf / fp8_peak, 4),
-                          "flops": units})
+                          "frac_fp8_nominal": round(tf / fp8_nominal, 4), "flops": units})
         kern[label] = entry
     top = max(kern, key=lambda k: kern[k]["us"])
     top_kind = {l: k for l, k, _ in wl.kernels}[top]

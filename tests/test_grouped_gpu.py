@@ -49,6 +49,37 @@ def test_grouped_small(F, sizes, out):
             assert_gemm_close(dn[r0:r1], ref[r0:r1], na, nb, out)
 
 
+def test_grouped_max_experts_and_empty(F):
+    """E = 1024 (the limit) with 0-3 rows per expert, K = N = 128: every output
+    against the per-expert oracle; an empty problem (Mtot = 0) is a no-op."""
+    E, K, N = 1024, 128, 128
+    g = np.random.default_rng(11)
+    sizes = g.integers(0, 4, E)
+    offs = torch.tensor(np.concatenate([[0], np.cumsum(sizes)]), dtype=torch.int32)
+    Mtot = int(offs[-1])
+    a = W.bf16_normal((Mtot, K), 1.0, seed=12).cuda()
+    qa, sa = F.quant_act_1x128(a)
+    w = W.bf16_normal((E, K, N), 0.02, seed=13)
+    qb = torch.empty((E, N, K), dtype=torch.uint8, device="cuda")
+    sb = torch.empty((E, 1, 1), dtype=torch.float32, device="cuda")
+    for e in range(E):
+        F.quant_w_128x128(w[e].cuda(), q=qb[e], sb=sb[e])
+    d = F.grouped_gemm(qa, sa, offs.cuda(), qb, sb, out_dtype=torch.float32)
+    assert F.get_status() == F.OK
+    qa_n, sa_n, qb_n, sb_n, o, dn = (qa.cpu().numpy(), sa.cpu().numpy(), qb.cpu().numpy(),
+                                     sb.cpu().numpy(), offs.numpy(), to_np(d))
+    for e in range(E):
+        r0, r1 = int(o[e]), int(o[e + 1])
+        if r1 > r0:
+            ref = O.gemm_blockscaled(qa_n[r0:r1], sa_n[:, r0:r1], qb_n[e], sb_n[e])
+            na, nb = O.row_col_norms(qa_n[r0:r1], sa_n[:, r0:r1], qb_n[e], sb_n[e])
+            assert_gemm_close(dn[r0:r1], ref, na, nb, "f32")
+    empty = torch.empty((0, K), dtype=torch.uint8, device="cuda")
+    z = F.grouped_gemm(empty, torch.empty((1, 0), device="cuda"),
+                       torch.zeros(E + 1, dtype=torch.int32, device="cuda"), qb, sb)
+    assert z.shape == (0, N) and F.get_status() == F.OK
+
+
 def _moe_check_sampled(F, p, rows_per_expert):
     x, w, rows, offs = p.make()
     qx, sx = F.quant_act_1x128(x.cuda(), True)            # quantize before dispatch
