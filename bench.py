@@ -67,7 +67,8 @@ def parse_args(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="dense_fwd",
                     choices=["dense_fwd", "square", "dgrad", "moe", "moe_scatter", "moe_gather",
-                             "moe_decode", "moe_act_grad", "wgrad", "ksweep", "quant"])
+                             "moe_decode", "moe_act_grad", "wgrad", "ksweep", "quant", "mx",
+                             "mx_square", "moe_mx"])
     ap.add_argument("--legs", default="device,e2e,cpu",
                     help="measurement legs to run: device (always), e2e, cpu")
     a = ap.parse_args(argv)
@@ -159,12 +160,14 @@ class Workload:
 
 
 class DenseForward(Workload):
-    """quant_act(A) -> quant_w(W) -> GEMM, bf16 out."""
+    """quant_act(A) -> quant_w(W) -> GEMM, bf16 out. mx: power-of-two scales
+    and the GEMM with the tensor cores' UE8M0 block scaling (no promotion)."""
 
-    def __init__(self, problem, device):
+    def __init__(self, problem, device, mx=False):
         import torch
         from fp8_block_scaled_17_b300 import fp8q as F
         self.F, self.torch, self.p = F, torch, problem
+        self.mx = mx
         M, N, K = problem.M, problem.N, problem.K
         a, w = problem.make()
         self.a_host, self.w_host = a, w
@@ -174,23 +177,32 @@ class DenseForward(Workload):
         self.qb = torch.empty((N, K), dtype=torch.uint8, device=device)
         self.sb = torch.empty((K // 128, N // 128), dtype=torch.float32, device=device)
         self.d = torch.empty((M, N), dtype=torch.bfloat16, device=device)
+        gemm_desc = ("block-scaled FP8 GEMM promoted every 128 K" if not mx else
+                     "FP8 GEMM with the scales applied as UE8M0 block scales inside the "
+                     "tensor core (kind::mxf8f6f4), no promotion")
         self.name = (f"dense forward Linear: A [{M}][{K}] bf16 (0.1% x{problem.a_outlier_scale:g} "
-                     f"outliers) quantized 1x128, W [{K}][{N}] bf16 quantized 128x128, "
-                     f"block-scaled FP8 GEMM promoted every 128 K, bf16 D [{M}][{N}]")
+                     f"outliers) quantized 1x128, W [{K}][{N}] bf16 quantized 128x128"
+                     f"{', power-of-two scales' if mx else ''}, {gemm_desc}, bf16 D [{M}][{N}]")
         self.flops = problem.flops
-        self.kernels = [("quant_act_1x128", "hbm", M * K * (2 + 1 + 4 / 128)),
-                        ("quant_w_128x128", "hbm", K * N * (2 + 1 + 4 / 16384)),
-                        ("gemm_blockscaled", "tensor", problem.flops)]
+        sfx = "_pow2" if mx else ""
+        self.kernels = [("quant_act_1x128" + sfx, "hbm", M * K * (2 + 1 + 4 / 128)),
+                        ("quant_w_128x128" + sfx, "hbm", K * N * (2 + 1 + 4 / 16384)),
+                        ("gemm_mx" if mx else "gemm_blockscaled", "tensor", problem.flops)]
         self.config = {"M": M, "N": N, "K": K, "out": "bf16", "a_scale": "1x128",
-                       "b_scale": "128x128", "promotion_interval": 128}
+                       "b_scale": "128x128"}
+        if mx:
+            self.config.update({"scales": "pow2, UE8M0 in the tensor core",
+                                "promotion_interval": None})
+        else:
+            self.config["promotion_interval"] = 128
         self.h2d_bytes = a.numel() * 2 + w.numel() * 2
         self.d2h_bytes = M * N * 2
 
     def calls(self):
-        F = self.F
-        return [lambda: F.quant_act_1x128(self.a, q=self.qa, sa=self.sa),
-                lambda: F.quant_w_128x128(self.w, q=self.qb, sb=self.sb),
-                lambda: F.gemm_blockscaled(self.qa, self.sa, self.qb, self.sb, d=self.d)]
+        F, mx = self.F, self.mx
+        return [lambda: F.quant_act_1x128(self.a, mx, q=self.qa, sa=self.sa),
+                lambda: F.quant_w_128x128(self.w, mx, q=self.qb, sb=self.sb),
+                lambda: F.gemm_blockscaled(self.qa, self.sa, self.qb, self.sb, d=self.d, mx=mx)]
 
     def e2e_setup(self):
         """Pinned host A, W and D; two device sets of A, W and D so that step i+1's
@@ -222,11 +234,11 @@ class DenseForward(Workload):
             self.Wd[k].copy_(self.pw, non_blocking=True)
             self.in_ready[k].record(self.s_up)
         comp.wait_event(self.in_ready[k])
-        F.quant_act_1x128(self.A[k], q=self.qa, sa=self.sa)
-        F.quant_w_128x128(self.Wd[k], q=self.qb, sb=self.sb)
+        F.quant_act_1x128(self.A[k], self.mx, q=self.qa, sa=self.sa)
+        F.quant_w_128x128(self.Wd[k], self.mx, q=self.qb, sb=self.sb)
         self.in_free[k].record(comp)
         comp.wait_event(self.out_free[k])  # the download of step i-2 read D[k]
-        F.gemm_blockscaled(self.qa, self.sa, self.qb, self.sb, d=self.D[k])
+        F.gemm_blockscaled(self.qa, self.sa, self.qb, self.sb, d=self.D[k], mx=self.mx)
         self.out_ready[k].record(comp)
         with torch.cuda.stream(self.s_down):
             self.s_down.wait_event(self.out_ready[k])
@@ -243,8 +255,8 @@ class DenseForward(Workload):
         a = self.a_host[:rows].float().numpy()
         w = self.w_host[:, :cols].float().numpy()
         t0 = time.perf_counter()
-        qa, sa = O.quant_act_1x128(a)
-        qb, sb = O.quant_w_128x128(w)
+        qa, sa = O.quant_act_1x128(a, self.mx)
+        qb, sb = O.quant_w_128x128(w, self.mx)
         O.gemm_blockscaled(qa, sa, qb, sb)
         dt = time.perf_counter() - t0
         flops = 2.0 * rows * cols * self.p.K
@@ -255,7 +267,7 @@ class DenseForward(Workload):
 class MoeGrouped(Workload):
     """quant_act(tokens, pow2) -> grouped GEMM over expert-sorted rows."""
 
-    def __init__(self, problem, device, decode=False, gather=False, scatter=False):
+    def __init__(self, problem, device, decode=False, gather=False, scatter=False, mx=False):
         import torch
         from fp8_block_scaled_17_b300 import fp8q as F
         from fp8_block_scaled_17_b300 import workloads as W
@@ -279,16 +291,20 @@ class MoeGrouped(Workload):
         self.offs = offs.to(device)
         self.qb = torch.empty((E, N, K), dtype=torch.uint8, device=device)
         self.sb = torch.empty((E, K // 128, N // 128), dtype=torch.float32, device=device)
+        self.mx = mx  # power-of-two weight scales, UE8M0 block scaling in the GEMM
         for e in range(E):
-            F.quant_w_128x128(w[e].to(device), q=self.qb[e], sb=self.sb[e])
+            F.quant_w_128x128(w[e].to(device), mx, q=self.qb[e], sb=self.sb[e])
         self.d = torch.empty((problem.rows, N), dtype=torch.bfloat16, device=device)
         self.name = getattr(self, "name", problem.name)
         if gather:
             self.name = problem.name + " (dispatch gather fused into the GEMM)"
         if scatter:
             self.name = problem.name + " (dispatch fused into the quantizer)"
+        if mx:
+            self.name = (problem.name + " (power-of-two weight scales; the grouped GEMM with "
+                         "UE8M0 block scaling in the tensor core, no promotion)")
         self.flops = problem.flops
-        gemm = ("grouped_gemm", "tensor", problem.flops)
+        gemm = ("grouped_gemm_mx" if mx else "grouped_gemm", "tensor", problem.flops)
         if decode:  # weight-bandwidth bound: algorithmic bytes of codes, scales and D
             gemm = ("grouped_gemm", "hbm",
                     E * N * K + problem.rows * K + problem.rows * N * 2
@@ -314,7 +330,8 @@ class MoeGrouped(Workload):
                     lambda: F.grouped_gemm_gather(self.qx, self.sx, self.rows_i32, self.offs,
                                                   self.qb, self.sb, d=self.d)]
         return [lambda: F.quant_act_1x128(self.x, True, q=self.qx, sa=self.sx),
-                lambda: F.grouped_gemm(self.qa, self.sa, self.offs, self.qb, self.sb, d=self.d)]
+                lambda: F.grouped_gemm(self.qa, self.sa, self.offs, self.qb, self.sb, d=self.d,
+                                       mx=self.mx)]
 
 
 class MoeActGrad(Workload):
@@ -493,6 +510,12 @@ def make_workload(name, device):
         return DenseForward(W.DENSE_FWD, device)
     if name == "square":
         return DenseForward(W.SQUARE_8K, device)
+    if name == "mx":
+        return DenseForward(W.DENSE_FWD, device, mx=True)
+    if name == "mx_square":
+        return DenseForward(W.SQUARE_8K, device, mx=True)
+    if name == "moe_mx":
+        return MoeGrouped(W.MoeProblem(), device, mx=True)
     if name == "dgrad":
         return Dgrad(W.DgradProblem(), device)
     if name == "moe":
@@ -779,6 +802,7 @@ def run_reference(args):
     host = _Host()
     host.a_host, host.w_host = p.make()
     host.p = p
+    host.mx = False
     sample = DenseForward.cpu_sample
     for _ in range(args.warmup):
         sample(host, rows=16, cols=256)

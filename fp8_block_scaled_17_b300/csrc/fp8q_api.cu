@@ -11,6 +11,7 @@
 
 #include "fp8q.h"
 #include "gemm.cuh"
+#include "gemm_mx.cuh"
 #include "ptx.cuh"
 #include "quant.cuh"
 
@@ -30,6 +31,7 @@ struct DeviceInfo {
   bool supported = false;
   bool gemm_ok = false;     // BN = 128 GEMM can be launched with 384 threads
   bool gemm256_ok = false;  // BN = 256: its register split matches the compiled count
+  bool gemm_mx_ok = false;  // block-scaled MMA kernel can be launched with its 352 threads
   int num_sms = 0;
   unsigned* status = nullptr;
   // resident CTAs per SM of the persistent quantizer kernels
@@ -83,6 +85,12 @@ fp8q_status device_info(DeviceInfo** out) {
         return FP8Q_ERR_CUDA;
       d.gemm_ok = fa128.maxThreadsPerBlock >= kThreads;
       d.gemm256_ok = fa256.numRegs == kLaunchRegs && fa256.maxThreadsPerBlock >= kThreads;
+      cudaFuncAttributes fa_mx;
+      if (cudaFuncSetAttribute(gemm_mx_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(mx::smem_bytes(kMaxExperts))) != cudaSuccess ||
+          cudaFuncGetAttributes(&fa_mx, gemm_mx_kernel) != cudaSuccess)
+        return FP8Q_ERR_CUDA;
+      d.gemm_mx_ok = fa_mx.maxThreadsPerBlock >= mx::kThreads;
       using namespace fp8q;
       const int rs = kRowSmemBytes, cs0 = col_smem_bytes<0>(), cs1 = col_smem_bytes<1>();
       d.occ_rows = d.occ_cols_bf16 = d.occ_cols_codes = d.occ_blocks = 1;
@@ -159,9 +167,14 @@ fp8q_status gemm_common(const uint8_t* A, const float* sa, int64_t a_rows,
                         void* D, int64_t ldd, unsigned flags, cudaStream_t stream) {
   using namespace fp8q::gemm;
   const bool grouped = m_offsets != nullptr;
-  const unsigned allowed = grouped ? (FP8Q_OUT_BF16 | FP8Q_NO_PROMOTION)
-                                   : (FP8Q_OUT_BF16 | FP8Q_NO_PROMOTION | FP8Q_SCALE_B_1x128);
+  const unsigned allowed =
+      grouped ? (FP8Q_OUT_BF16 | FP8Q_NO_PROMOTION | FP8Q_MX_BLOCK_SCALE)
+              : (FP8Q_OUT_BF16 | FP8Q_NO_PROMOTION | FP8Q_SCALE_B_1x128 | FP8Q_MX_BLOCK_SCALE);
   if (flags & ~allowed) return FP8Q_ERR_INVALID_ARG;
+  const bool mx_scale = (flags & FP8Q_MX_BLOCK_SCALE) != 0;
+  // the block-scaled MMA has no promotion to turn off; it reads A rows in order
+  if (mx_scale && (flags & FP8Q_NO_PROMOTION)) return FP8Q_ERR_INVALID_ARG;
+  if (mx_scale && row_index) return FP8Q_ERR_UNSUPPORTED;
   if (M < 0 || N <= 0 || K <= 0 || N % 128 || K % 128) return FP8Q_ERR_SHAPE;
   if (ldd < N) return FP8Q_ERR_SHAPE;
   if (E < 1 || E > kMaxExperts) return FP8Q_ERR_SHAPE;
@@ -181,9 +194,11 @@ fp8q_status gemm_common(const uint8_t* A, const float* sa, int64_t a_rows,
   DeviceInfo* dev = nullptr;
   if (fp8q_status st = device_info(&dev)) return st;
   // CTA tile N: 256 (two TMEM accumulator buffers) unless FP8Q_GEMM_TILE_N=128
+  // (the block-scaled MMA kernel always uses 256)
   const char* tn = std::getenv("FP8Q_GEMM_TILE_N");
-  const int bn = (tn && std::strcmp(tn, "128") == 0) ? 128 : 256;
-  if (bn == 128 ? !dev->gemm_ok : !dev->gemm256_ok) return FP8Q_ERR_UNSUPPORTED;
+  const int bn = (!mx_scale && tn && std::strcmp(tn, "128") == 0) ? 128 : 256;
+  if (mx_scale ? !dev->gemm_mx_ok : (bn == 128 ? !dev->gemm_ok : !dev->gemm256_ok))
+    return FP8Q_ERR_UNSUPPORTED;
 
   // a gathered A tile is 32 tile::gather4 loads of four one-row boxes
   const uint32_t box_a_rows = row_index ? 1u : static_cast<uint32_t>(M < BM ? M : BM);
@@ -222,7 +237,9 @@ fp8q_status gemm_common(const uint8_t* A, const float* sa, int64_t a_rows,
     const int64_t tiles = ((M + BM - 1) / BM) * ((N + bn - 1) / bn);
     if (tiles < grid) grid = static_cast<int>(tiles);
   }
-  if (bn == 128) {
+  if (mx_scale) {
+    gemm_mx_kernel<<<grid, mx::kThreads, mx::smem_bytes(E), stream>>>(tmA, tmB, p);
+  } else if (bn == 128) {
     gemm_blockscaled_kernel<128><<<grid, kThreads, Cfg<128>::bytes(E), stream>>>(tmA, tmB, p);
   } else {
     gemm_blockscaled_kernel<256><<<grid, kThreads, Cfg<256>::bytes(E), stream>>>(tmA, tmB, p);
@@ -398,7 +415,7 @@ FP8Q_API fp8q_status fp8q_get_status(fp8q_stream_t stream) {
       return FP8Q_ERR_CUDA;
   }
   if (v & fp8q::kDevStatusTimeout) return FP8Q_ERR_TIMEOUT;
-  if (v & fp8q::kDevStatusBadOffsets) return FP8Q_ERR_INVALID_ARG;
+  if (v & (fp8q::kDevStatusBadOffsets | fp8q::kDevStatusBadScale)) return FP8Q_ERR_INVALID_ARG;
   return FP8Q_OK;
 }
 

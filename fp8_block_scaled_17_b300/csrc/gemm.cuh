@@ -53,6 +53,7 @@ namespace fp8q {
 // Error bits recorded by kernels (read and cleared by fp8q_get_status).
 constexpr unsigned kDevStatusTimeout = 1u;
 constexpr unsigned kDevStatusBadOffsets = 2u;  // also: gather indices out of range
+constexpr unsigned kDevStatusBadScale = 4u;    // block-scaled MMA: a scale is not a power of two
 
 namespace gemm {
 
@@ -237,6 +238,76 @@ __device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
   return d;
 }
 
+// Tile schedule tables, first half: seg[e] = m_offsets[e] (a dense GEMM is
+// one segment [0, M]). All threads of the block; a barrier must follow.
+__device__ __forceinline__ void load_segments(const Params& p, int* seg) {
+  for (int e = threadIdx.x; e <= p.E; e += blockDim.x)
+    seg[e] = p.m_offsets ? __ldg(p.m_offsets + e) : (e == 0 ? 0 : static_cast<int>(p.M));
+}
+
+// Second half, one thread: clamp the segment offsets into [0, M],
+// nondecreasing (reporting offsets that needed it) and count the tiles before
+// each expert: pre[e]; pre[E] is the number of tiles.
+__device__ __forceinline__ void finish_segments(const Params& p, int* seg, int* pre, int nt) {
+  const int M = static_cast<int>(p.M);
+  bool bad = false;
+  int prev = 0;
+  for (int e = 0; e <= p.E; ++e) {
+    int v = seg[e];
+    if ((e == 0 && v != 0) || (e == p.E && v != M)) bad = true;
+    if (e == 0) v = 0;
+    if (e == p.E) v = M;
+    if (v < prev) { bad = true; v = prev; }
+    if (v > M) { bad = true; v = M; }
+    seg[e] = v;
+    prev = v;
+  }
+  pre[0] = 0;
+  for (int e = 0; e < p.E; ++e) pre[e + 1] = pre[e] + ((seg[e + 1] - seg[e] + BM - 1) / BM) * nt;
+  if (bad && blockIdx.x == 0) atomicOr(p.status, kDevStatusBadOffsets);
+}
+
+// TMA producer (one thread): for every K-block of every tile of this CTA, one
+// A box (128 rows) and one B box (BN rows) into the next stage of the ring.
+// full barrier of stage s at bars + 8 s, empty barrier at bars + 8 (kStages + s).
+template <int BN, int kStages>
+__device__ __forceinline__ void produce_tiles(const CUtensorMap* tmA, const CUtensorMap* tmB,
+                                              const Params& p, const int* seg, const int* pre,
+                                              int total, int nt, int KB, uint32_t a_base,
+                                              uint32_t b_base, uint32_t bars,
+                                              volatile uint32_t* abort_flag) {
+  auto full_bar = [&](int s) { return bars + 8u * s; };
+  auto empty_bar = [&](int s) { return bars + 8u * (kStages + s); };
+  int stage = 0;
+  uint32_t phase = 0;
+  int issued = 0;
+  bool ok = true;
+  for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+    const Tile tl = tile_at(t, seg, pre, p.E, nt, p.N, p.group_m, BN);
+    for (int kb = 0; kb < KB; ++kb) {
+      if (!wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, p, p.wait_limit_ns)) {
+        ok = false;
+        break;
+      }
+      mbar_arrive_expect_tx(full_bar(stage), p.tx_bytes);
+      tma_load_2d(a_base + stage * kABytes, tmA, full_bar(stage), kb * BK,
+                  static_cast<int32_t>(tl.m0));
+      tma_load_2d(b_base + stage * (BN * BK), tmB, full_bar(stage), kb * BK, tl.brow0);
+      ++issued;
+      if (++stage == kStages) { stage = 0; phase ^= 1u; }
+    }
+  }
+  if (!ok) {  // let the loads still in flight land before the CTA exits
+    const int n = issued < kStages ? issued : kStages;
+    for (int i = 1; i <= n; ++i) {
+      int s = stage - i;
+      uint32_t ph = phase;
+      if (s < 0) { s += kStages; ph ^= 1u; }
+      wait_drain(full_bar(s), ph, p.wait_limit_ns);
+    }
+  }
+}
+
 template <int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_blockscaled_kernel(const __grid_constant__ CUtensorMap tmA,
@@ -272,9 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool promote = (p.flags & kFlagPromote) != 0;
 
   // ---------------------------------------------------------------- setup
-  for (int e = threadIdx.x; e <= p.E; e += kThreads) {
-    seg[e] = p.m_offsets ? __ldg(p.m_offsets + e) : (e == 0 ? 0 : static_cast<int>(p.M));
-  }
+  load_segments(p, seg);
   if (warp == kMmaWarp) {
     tmem_alloc(base + C::misc_off, kTmemCols);
     tmem_relinquish();
@@ -302,25 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&tmB);
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    // Clamp the segment offsets into [0, M], nondecreasing, and count tiles.
-    const int M = static_cast<int>(p.M);
-    bool bad = false;
-    int prev = 0;
-    for (int e = 0; e <= p.E; ++e) {
-      int v = seg[e];
-      if ((e == 0 && v != 0) || (e == p.E && v != M)) bad = true;
-      if (e == 0) v = 0;
-      if (e == p.E) v = M;
-      if (v < prev) { bad = true; v = prev; }
-      if (v > M) { bad = true; v = M; }
-      seg[e] = v;
-      prev = v;
-    }
-    pre[0] = 0;
-    for (int e = 0; e < p.E; ++e) pre[e + 1] = pre[e] + ((seg[e + 1] - seg[e] + BM - 1) / BM) * nt;
-    if (bad && blockIdx.x == 0) atomicOr(p.status, kDevStatusBadOffsets);
-  }
+  if (threadIdx.x == 0) finish_segments(p, seg, pre, nt);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -384,37 +435,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
     } else if (warp == kProducerWarp) {
       // ----------------------------------------------------- TMA producer
-      if (lane == 0) {
-        int stage = 0;
-        uint32_t phase = 0;
-        int issued = 0;
-        bool ok = true;
-        for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-          const Tile tl = tile_at(t, seg, pre, p.E, nt, p.N, p.group_m, BN);
-          for (int kb = 0; kb < KB; ++kb) {
-            if (!wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, p, p.wait_limit_ns)) {
-              ok = false;
-              break;
-            }
-            mbar_arrive_expect_tx(full_bar(stage), p.tx_bytes);
-            tma_load_2d(base + C::a_off + stage * kABytes, &tmA, full_bar(stage), kb * BK,
-                        static_cast<int32_t>(tl.m0));
-            tma_load_2d(base + C::b_off + stage * C::kBBytes, &tmB, full_bar(stage), kb * BK,
-                        tl.brow0);
-            ++issued;
-            if (++stage == kStages) { stage = 0; phase ^= 1u; }
-          }
-        }
-        if (!ok) {  // let the loads still in flight land before the CTA exits
-          const int n = issued < kStages ? issued : kStages;
-          for (int i = 1; i <= n; ++i) {
-            int s = stage - i;
-            uint32_t ph = phase;
-            if (s < 0) { s += kStages; ph ^= 1u; }
-            wait_drain(full_bar(s), ph, p.wait_limit_ns);
-          }
-        }
-      }
+      if (lane == 0)
+        produce_tiles<BN, kStages>(&tmA, &tmB, p, seg, pre, total, nt, KB, base + C::a_off,
+                                   base + C::b_off, bar0, abort_flag);
       __syncwarp();
     } else if (warp == kMmaWarp) {
       // --------------------------------------------------------- MMA issuer

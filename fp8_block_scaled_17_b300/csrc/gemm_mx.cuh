@@ -1,0 +1,382 @@
+// Block-scaled FP8 GEMM on the tensor cores' own block scaling: the
+// microscaling counterpart of the promoted kernel in gemm.cuh ("Don't Be
+// Fooled By Deepseek Chatgpt" and why-be.co.kr board post 61844, paragraph
+// relating the fine-grained tile/block quantization to microscaling formats,
+// which Blackwell tensor cores support with smaller groups).
+//
+// tcgen05.mma kind::mxf8f6f4 multiplies every 32-element K slice of a row of A
+// and of a row of B by a UE8M0 scale (a power of two) inside the tensor core
+// and accumulates all of K in TMEM: there is no promotion step. A power-of-two
+// 1x128 activation scale or 128x128 weight-block scale is that scale repeated
+// over the four 32-element slices of its 128 K, so the result equals the
+// promoted GEMM's up to the rounding of the accumulation. A scale that is not
+// a positive normal power of two has no UE8M0 form: the kernel reports it
+// (kDevStatusBadScale) and uses its exponent bits.
+//
+// Scale factors in tensor memory, M = 128 (as measured on sm_103a with a
+// one-instruction layout probe): the A scale of output row m is read from lane
+// m, column sfa + m/32; the B scale of output column n from column
+// sfb + n/32 in lane n % 32 of a lane quarter; in both, the byte of the 32-bit
+// word that the instruction descriptor's scale-factor ID names. One word thus
+// holds four scales: the kernel packs the scales of four consecutive K-blocks
+// into its bytes and K-block kb uses ID kb % 4. A group of four K-blocks takes
+// 4 TMEM columns for A and BN/32 = 8 for B.
+//
+// Path of the scales: warp 10 reads the FP32 scales of a group of four
+// K-blocks, converts them to UE8M0 and writes three blocks of 32 rows x 16
+// bytes into a shared-memory ring: row r of the A block holds the words of
+// tile rows r, r+32, r+64, r+96; row r of B block j (j = 0, 1) those of tile
+// columns 128j + 32c + r, c = 0..3. The MMA thread copies each block into
+// tensor memory with tcgen05.cp .32x128b.warpx4, which writes the 32 rows to
+// all four lane quarters, so word c of row r lands in lane 32q + r, column c:
+// the layout above. The copies execute in order with the MMAs the same thread
+// issues after them.
+//
+// Warp roles (352 threads, one CTA per SM, persistent over tiles):
+//   warps 0-7  epilogue: warp w loads lanes 32(w%4).. and columns 128(w/4)..
+//              of the accumulator into registers, releases it, rounds to bf16
+//              (or keeps FP32) and stores.
+//   warp 8     TMA producer (produce_tiles, as the promoted kernel).
+//   warp 9     TMEM allocator + MMA issuer (one thread).
+//   warp 10    scale converter.
+// TMEM: one 128 x 256 FP32 accumulator (columns 0-255) and kSfSlots groups of
+// scale columns. The epilogue holds the accumulator only while it loads it,
+// so the next tile's MMAs wait for four TMEM loads per warp, not for the
+// stores. Every wait is bounded as in gemm.cuh.
+#pragma once
+#include "gemm.cuh"
+
+namespace fp8q {
+namespace gemm {
+namespace mx {
+
+constexpr int BN = 256;
+constexpr int kStages = 4;
+constexpr int kEpiWarps = 8;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kSfWarp = 10;
+constexpr int kThreads = 352;
+constexpr int kSfSlots = 8;
+constexpr uint32_t kSfBlockBytes = 512;  // 32 rows x 16 bytes
+constexpr uint32_t kSfSlotBytes = 3 * kSfBlockBytes;
+constexpr uint32_t kAccCols = BN;
+constexpr uint32_t kSfaCol = kAccCols;                 // 4 columns per slot
+constexpr uint32_t kSfbCol = kSfaCol + 4 * kSfSlots;  // 8 columns per slot
+static_assert(kSfbCol + 8 * kSfSlots <= kTmemCols, "TMEM columns");
+
+// shared memory layout (offsets from a 1024-byte aligned base)
+constexpr uint32_t a_off = 0;
+constexpr uint32_t b_off = a_off + kStages * kABytes;
+constexpr uint32_t sf_off = b_off + kStages * BN * BK;
+constexpr uint32_t bar_off = sf_off + kSfSlots * kSfSlotBytes;
+constexpr uint32_t n_bars = 2 * kStages + 2 + 2 * kSfSlots + 2;
+constexpr uint32_t misc_off = bar_off + n_bars * 8;  // tmem base, abort flag
+constexpr uint32_t table_off = misc_off + 16;        // seg[E+1], prefix[E+1]
+__host__ __device__ constexpr uint32_t smem_bytes(int E) { return table_off + 8u * (E + 1) + 1024u; }
+static_assert(smem_bytes(kMaxExperts) <= 232448, "shared memory budget");
+
+// UE8M0 code of a scale: its biased exponent. Anything but a positive normal
+// power of two sets `bad`.
+__device__ __forceinline__ uint32_t ue8m0(float s, bool& bad) {
+  const uint32_t u = __float_as_uint(s);
+  const uint32_t e = u >> 23;  // includes the sign bit: negative -> e >= 256
+  bad |= (u & 0x7FFFFFu) != 0u || e == 0u || e >= 255u;
+  return e & 0xFFu;
+}
+
+__device__ __forceinline__ uint32_t pack_bytes(uint32_t b0, uint32_t b1, uint32_t b2, uint32_t b3) {
+  return b0 | (b1 << 8) | (b2 << 16) | (b3 << 24);
+}
+
+}  // namespace mx
+
+__global__ void __launch_bounds__(mx::kThreads, 1)
+    gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const Params p) {
+  using namespace mx;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* const base_ptr = smem_raw + (base - raw);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  const uint32_t bar0 = base + bar_off;
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (kStages + s); };
+  const uint32_t tfull_bar = bar0 + 8u * (2 * kStages);
+  const uint32_t tempty_bar = tfull_bar + 8u;
+  auto sf_full_bar = [&](uint32_t i) { return tempty_bar + 8u * (1 + i); };
+  auto sf_empty_bar = [&](uint32_t i) { return tempty_bar + 8u * (1 + kSfSlots + i); };
+  const uint32_t drain_bar = tempty_bar + 8u * (1 + 2 * kSfSlots);
+  const uint32_t never_bar = drain_bar + 8u;
+  uint32_t* const misc = reinterpret_cast<uint32_t*>(base_ptr + misc_off);
+  volatile uint32_t* const abort_flag = misc + 1;
+  int* const seg = reinterpret_cast<int*>(base_ptr + table_off);
+  int* const pre = seg + (p.E + 1);
+
+  const int nt = (p.N + BN - 1) / BN;
+  const int KB = p.K / BK;
+  const int groups = (KB + 3) / 4;  // scale groups per tile
+
+  // ---------------------------------------------------------------- setup
+  load_segments(p, seg);
+  if (warp == mx::kMmaWarp) {
+    tmem_alloc(base + misc_off, kTmemCols);
+    tmem_relinquish();
+  }
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    mbar_init(tfull_bar, 1);
+    mbar_init(tempty_bar, kEpiWarps);
+    for (uint32_t i = 0; i < kSfSlots; ++i) {
+      mbar_init(sf_full_bar(i), 1);
+      mbar_init(sf_empty_bar(i), 1);
+    }
+    mbar_init(drain_bar, 1);
+    mbar_init(never_bar, 1);
+    misc[1] = 0u;
+    fence_mbar_init();
+  }
+  if (warp == mx::kProducerWarp && lane == 0) {
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) finish_segments(p, seg, pre, nt);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = misc[0];
+  const int total = pre[p.E];
+  const bool sb1 = (p.flags & kFlagScaleB1x128) != 0;
+  const int NB = p.N / 128;
+
+  if (warp == mx::kProducerWarp) {
+    // ------------------------------------------------------- TMA producer
+    if (lane == 0)
+      produce_tiles<BN, kStages>(&tmA, &tmB, p, seg, pre, total, nt, KB, base + a_off,
+                                 base + b_off, bar0, abort_flag);
+    __syncwarp();
+  } else if (warp == mx::kMmaWarp) {
+    // --------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t gslot = 0, gphase = 0;  // scale ring position
+      uint32_t tiles = 0;
+      bool ok = true;
+      if (p.inject_timeout) ok = wait_bounded(never_bar, 0u, abort_flag, p, 20000000ull);
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++tiles) {
+        // the epilogue has read the previous tile's accumulator
+        if (!wait_bounded(tempty_bar, (tiles & 1u) ^ 1u, abort_flag, p, p.wait_limit_ns)) {
+          ok = false;
+          break;
+        }
+        for (int kb = 0; kb < KB; ++kb) {
+          const uint32_t kk = static_cast<uint32_t>(kb) & 3u;
+          if (kk == 0 &&
+              !wait_bounded(sf_full_bar(gslot), gphase, abort_flag, p, p.wait_limit_ns)) {
+            ok = false;
+            break;
+          }
+          if (!wait_bounded(full_bar(stage), phase, abort_flag, p, p.wait_limit_ns)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sfa = tmem_base + kSfaCol + 4u * gslot;
+          const uint32_t sfb = tmem_base + kSfbCol + 8u * gslot;
+          if (kk == 0) {
+            const uint32_t src = base + sf_off + gslot * kSfSlotBytes;
+            tmem_cp_32x128b_warpx4(sfa, plain_rows16_desc(src));
+            tmem_cp_32x128b_warpx4(sfb, plain_rows16_desc(src + kSfBlockBytes));
+            tmem_cp_32x128b_warpx4(sfb + 4u, plain_rows16_desc(src + 2 * kSfBlockBytes));
+          }
+          const uint64_t adesc = sw128_kmajor_desc(base + a_off + stage * kABytes);
+          const uint64_t bdesc = sw128_kmajor_desc(base + b_off + stage * (BN * BK));
+          const uint32_t idesc = idesc_mx_e4m3(BM, BN, kk, kk);
+#pragma unroll
+          for (int k = 0; k < BK / 32; ++k)
+            umma_mx_f8f6f4(tmem_base, adesc + 2u * k, bdesc + 2u * k, idesc, sfa, sfb,
+                           (kb > 0 || k > 0) ? 1u : 0u);
+          umma_commit(empty_bar(stage));
+          if (kk == 3 || kb == KB - 1) {  // the group's scales are no longer read
+            umma_commit(sf_empty_bar(gslot));
+            if (++gslot == kSfSlots) { gslot = 0; gphase ^= 1u; }
+          }
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        umma_commit(tfull_bar);
+      }
+      if (!ok) {  // wait for the MMAs and copies already issued
+        umma_commit(drain_bar);
+        wait_drain(drain_bar, 0u, p.wait_limit_ns);
+      }
+    }
+    __syncwarp();
+  } else if (warp == kSfWarp) {
+    // ---------------------------------------------------- scale converter
+    uint32_t gslot = 0, gphase = 0;
+    bool ok = true, bad = false;
+    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      const Tile tl = tile_at(t, seg, pre, p.E, nt, p.N, p.group_m, BN);
+      const int64_t left = tl.m_end - tl.m0;
+      const int rows = left < BM ? static_cast<int>(left) : BM;
+      const int cols = p.N - tl.n0;
+      int32_t ar[4];  // A rows of this lane's tile rows lane + 32 i
+#pragma unroll
+      for (int i = 0; i < 4; ++i) ar[i] = a_row_quiet(p, tl, tl.m0 + lane + 32 * i);
+      const float* sb_blk = p.sb + static_cast<int64_t>(tl.e) * KB * NB + tl.n0 / 128;
+      for (int g = 0; g < groups; ++g) {
+        // FP32 scales of K-blocks 4g .. 4g+3 (1.0 where outside the problem)
+        float a[4][4], b[4][8];
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const int kb = 4 * g + kk;
+          const bool in_k = kb < KB;
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            a[kk][i] = (in_k && 32 * i + lane < rows) ? __ldg(p.sa + static_cast<int64_t>(kb) * p.a_rows + ar[i])
+                                                      : 1.0f;
+          if (!sb1) {
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+              b[kk][j] = (in_k && 128 * j < cols) ? __ldg(sb_blk + static_cast<int64_t>(kb) * NB + j) : 1.0f;
+          } else {
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {  // column 32 c + lane of the tile
+              const int n = 32 * c + lane;
+              b[kk][c] = (in_k && n < cols) ? __ldg(p.sb + static_cast<int64_t>(kb) * p.N + tl.n0 + n)
+                                            : 1.0f;
+            }
+          }
+        }
+        bool w = true;
+        if (lane == 0)
+          w = wait_bounded(sf_empty_bar(gslot), gphase ^ 1u, abort_flag, p, p.wait_limit_ns);
+        if (!__shfl_sync(0xffffffffu, w, 0)) {
+          ok = false;
+          break;
+        }
+        const uint32_t dst = base + sf_off + gslot * kSfSlotBytes + 16u * lane;
+        uint32_t wa[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          wa[i] = pack_bytes(ue8m0(a[0][i], bad), ue8m0(a[1][i], bad), ue8m0(a[2][i], bad),
+                             ue8m0(a[3][i], bad));
+        st_shared_v4(dst, wa[0], wa[1], wa[2], wa[3]);
+        if (!sb1) {
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            const uint32_t v = pack_bytes(ue8m0(b[0][j], bad), ue8m0(b[1][j], bad),
+                                          ue8m0(b[2][j], bad), ue8m0(b[3][j], bad));
+            st_shared_v4(dst + kSfBlockBytes * (1 + j), v, v, v, v);
+          }
+        } else {
+          uint32_t wb[8];
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            wb[c] = pack_bytes(ue8m0(b[0][c], bad), ue8m0(b[1][c], bad), ue8m0(b[2][c], bad),
+                               ue8m0(b[3][c], bad));
+          st_shared_v4(dst + kSfBlockBytes, wb[0], wb[1], wb[2], wb[3]);
+          st_shared_v4(dst + 2 * kSfBlockBytes, wb[4], wb[5], wb[6], wb[7]);
+        }
+        fence_proxy_async_smem();  // visible to tcgen05.cp
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sf_full_bar(gslot));
+        if (++gslot == kSfSlots) { gslot = 0; gphase ^= 1u; }
+      }
+    }
+    if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(p.status, kDevStatusBadScale);
+  } else if (warp < kEpiWarps) {
+    // ----------------------------------------------------------- epilogue
+    const int q = warp & 3;   // TMEM lane quarter -> rows 32q .. 32q+31
+    const int h = warp >> 2;  // column half -> columns 128h ..
+    uint32_t tiles = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x, ++tiles) {
+      const Tile tl = tile_at(t, seg, pre, p.E, nt, p.N, p.group_m, BN);
+      const bool got = wait_bounded(tfull_bar, tiles & 1u, abort_flag, p, p.wait_limit_ns);
+      if (!__all_sync(0xffffffffu, got)) break;  // keeps the TMEM loads warp-uniform
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + h * 128u;
+      const int64_t m = tl.m0 + q * 32 + lane;
+      const int col0 = tl.n0 + h * 128;
+      const bool store = m < tl.m_end && col0 < p.N;
+      if (p.flags & kFlagOutBF16) {
+        uint32_t o[64];  // 128 bf16, column pairs
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t r0[32], r1[32];
+          tmem_ld_32x32b_x32(taddr + 64u * c, r0);
+          tmem_ld_32x32b_x32(taddr + 64u * c + 32u, r1);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            o[32 * c + j] = pack_bf16x2(__uint_as_float(r0[2 * j]), __uint_as_float(r0[2 * j + 1]));
+            o[32 * c + 16 + j] =
+                pack_bf16x2(__uint_as_float(r1[2 * j]), __uint_as_float(r1[2 * j + 1]));
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tempty_bar);
+        if (store) {
+          __nv_bfloat16* d = static_cast<__nv_bfloat16*>(p.D) + m * p.ldd + col0;
+          if (p.flags & kFlagStore32) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              st_global_v8(d + 16 * j, o[8 * j], o[8 * j + 1], o[8 * j + 2], o[8 * j + 3],
+                           o[8 * j + 4], o[8 * j + 5], o[8 * j + 6], o[8 * j + 7]);
+          } else {
+            uint4* d4 = reinterpret_cast<uint4*>(d);
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              d4[j] = make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+          }
+        }
+      } else {
+        uint32_t v[128];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t(&r)[32] = *reinterpret_cast<uint32_t(*)[32]>(v + 32 * c);
+          tmem_ld_32x32b_x32(taddr + 32u * c, r);
+        }
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tempty_bar);
+        if (store) {
+          float* d = static_cast<float*>(p.D) + m * p.ldd + col0;
+          if (p.flags & kFlagStore32) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              st_global_v8(d + 8 * j, v[8 * j], v[8 * j + 1], v[8 * j + 2], v[8 * j + 3],
+                           v[8 * j + 4], v[8 * j + 5], v[8 * j + 6], v[8 * j + 7]);
+          } else {
+            uint4* d4 = reinterpret_cast<uint4*>(d);
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              d4[j] = make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+          }
+        }
+      }
+    }
+  }
+
+  // ---------------------------------------------------------------- teardown
+  tc_fence_before();
+  __syncthreads();
+  if (warp == mx::kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+}  // namespace gemm
+}  // namespace fp8q

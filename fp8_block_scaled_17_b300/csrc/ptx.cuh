@@ -151,6 +151,39 @@ __device__ __forceinline__ void umma_f8f6f4(uint32_t d_tmem, uint64_t a_desc, ui
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// Block-scaled variant (kind::mxf8f6f4, one UE8M0 scale per 32 elements of K
+// for each row of A and each row of B): D (+)= (A x sA) (B x sB)^T. The scale
+// factors are read from tensor memory at sfa_tmem / sfb_tmem; the instruction
+// descriptor selects the byte of each 32-bit scale word (idesc_mx_e4m3).
+__device__ __forceinline__ void umma_mx_f8f6f4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                               uint32_t idesc, uint32_t sfa_tmem,
+                                               uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, "
+      "[%4], [%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+// Shared memory -> tensor memory copy of 32 rows x 16 bytes, written to the
+// 32 lanes of every lane quarter (columns taddr .. taddr+3). Executes in issue
+// order with the tcgen05.mma instructions of the same thread.
+__device__ __forceinline__ void tmem_cp_32x128b_warpx4(uint32_t taddr, uint64_t src_desc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(src_desc)
+               : "memory");
+}
+// Generic-proxy shared-memory writes of this thread become visible to the
+// async proxy (tcgen05.cp, TMA) after this fence.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+               "r"(d)
+               : "memory");
+}
 // Arrive (once) on `bar` when every tcgen05 operation issued so far by this
 // thread has completed.
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
@@ -191,12 +224,36 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t smem_addr) {
   return d;
 }
 
+// Shared-memory descriptor of a dense, unswizzled block of 16-byte rows (core
+// matrices of 8 rows x 16 bytes, 128 bytes apart in both directions): the
+// source of tmem_cp_32x128b_warpx4.
+__device__ __forceinline__ uint64_t plain_rows16_desc(uint32_t smem_addr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4);  // start address / 16
+  d |= static_cast<uint64_t>(128 >> 4) << 16;               // leading offset
+  d |= static_cast<uint64_t>(128 >> 4) << 32;               // stride offset: 8 rows
+  d |= static_cast<uint64_t>(1) << 46;                      // descriptor version
+  return d;                                                 // layout: no swizzle
+}
+
 // Instruction descriptor, kind::f8f6f4: D f32, A and B e4m3, both K-major.
 __host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
   return (1u << 4)                                  // D format: f32
          | (0u << 7) | (0u << 10)                   // A, B format: e4m3
          | (static_cast<uint32_t>(N >> 3) << 17)    // N / 8
          | (static_cast<uint32_t>(M >> 4) << 24);   // M / 16
+}
+
+// Instruction descriptor, kind::mxf8f6f4 with UE8M0 scales: A and B e4m3,
+// both K-major, D f32. sf_a / sf_b pick the byte of the 32-bit scale word that
+// the instruction uses for A and for B.
+__host__ __device__ constexpr uint32_t idesc_mx_e4m3(int M, int N, uint32_t sf_a, uint32_t sf_b) {
+  return (sf_b << 4)                                // B scale-factor byte
+         | (0u << 7) | (0u << 10)                   // A, B format: e4m3
+         | (static_cast<uint32_t>(N >> 3) << 17)    // N / 8
+         | (1u << 23)                               // scale type: UE8M0
+         | (static_cast<uint32_t>(M >> 4) << 24)    // M / 16
+         | (sf_a << 29);                            // A scale-factor byte
 }
 
 }  // namespace fp8q

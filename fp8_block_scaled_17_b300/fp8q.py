@@ -24,6 +24,7 @@ SCALE_B_1x128 = 4
 NO_PROMOTION = 8
 OUT_BF16 = 16
 W_KN_LAYOUT = 32
+MX_BLOCK_SCALE = 64
 
 EXPORTED = ("fp8q_quant_act_1x128", "fp8q_quant_act_1x128_scatter", "fp8q_quant_w_128x128", "fp8q_requant_1x128_to_128x1",
             "fp8q_gemm_blockscaled", "fp8q_grouped_gemm", "fp8q_grouped_gemm_gather",
@@ -165,8 +166,10 @@ def requant_1x128_to_128x1(q_in: torch.Tensor, s_in: torch.Tensor, pow2: bool = 
 # --------------------------------------------------------------------- GEMMs
 def gemm_blockscaled(a: torch.Tensor, sa: torch.Tensor, b: torch.Tensor, sb: torch.Tensor,
                      out_dtype=torch.bfloat16, scale_b_1x128: bool = False,
-                     no_promotion: bool = False, d: torch.Tensor | None = None, stream=None):
-    """codes a [M][K], b [N][K] with scales -> D [M][N] (bf16 or f32)."""
+                     no_promotion: bool = False, mx: bool = False,
+                     d: torch.Tensor | None = None, stream=None):
+    """codes a [M][K], b [N][K] with scales -> D [M][N] (bf16 or f32); mx: the
+    tensor cores apply the (power-of-two) scales as UE8M0 block scales."""
     assert a.dtype == torch.uint8 and b.dtype == torch.uint8
     assert a.is_contiguous() and b.is_contiguous() and sa.is_contiguous() and sb.is_contiguous()
     M, K = a.shape
@@ -174,7 +177,8 @@ def gemm_blockscaled(a: torch.Tensor, sa: torch.Tensor, b: torch.Tensor, sb: tor
     if d is None:
         d = torch.empty((M, N), dtype=out_dtype, device=a.device)
     flags = ((OUT_BF16 if d.dtype == torch.bfloat16 else 0) |
-             (SCALE_B_1x128 if scale_b_1x128 else 0) | (NO_PROMOTION if no_promotion else 0))
+             (SCALE_B_1x128 if scale_b_1x128 else 0) | (NO_PROMOTION if no_promotion else 0) |
+             (MX_BLOCK_SCALE if mx else 0))
     _check(LIB.fp8q_gemm_blockscaled(_ptr(a), _ptr(sa), _ptr(b), _ptr(sb), M, N, K, _ptr(d),
                                      d.stride(0), flags, _stream(stream)),
            "fp8q_gemm_blockscaled")
@@ -183,7 +187,7 @@ def gemm_blockscaled(a: torch.Tensor, sa: torch.Tensor, b: torch.Tensor, sb: tor
 
 def grouped_gemm(a: torch.Tensor, sa: torch.Tensor, m_offsets: torch.Tensor, b: torch.Tensor,
                  sb: torch.Tensor, out_dtype=torch.bfloat16, no_promotion: bool = False,
-                 d: torch.Tensor | None = None, stream=None):
+                 mx: bool = False, d: torch.Tensor | None = None, stream=None):
     """expert-sorted codes a [Mtot][K], m_offsets int32 [E+1] (device),
     b [E][N][K], sb [E][K/128][N/128] -> D [Mtot][N]."""
     assert m_offsets.dtype == torch.int32 and m_offsets.is_cuda
@@ -193,7 +197,8 @@ def grouped_gemm(a: torch.Tensor, sa: torch.Tensor, m_offsets: torch.Tensor, b: 
     if d is None:
         d = torch.empty((Mtot, N), dtype=out_dtype, device=a.device)
     assert d.is_contiguous()
-    flags = (OUT_BF16 if d.dtype == torch.bfloat16 else 0) | (NO_PROMOTION if no_promotion else 0)
+    flags = ((OUT_BF16 if d.dtype == torch.bfloat16 else 0) |
+             (NO_PROMOTION if no_promotion else 0) | (MX_BLOCK_SCALE if mx else 0))
     _check(LIB.fp8q_grouped_gemm(_ptr(a), _ptr(sa), _ptr(m_offsets), E, _ptr(b), _ptr(sb), Mtot,
                                  N, K, _ptr(d), flags, _stream(stream)), "fp8q_grouped_gemm")
     return d

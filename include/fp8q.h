@@ -68,7 +68,8 @@ enum {
   FP8Q_SCALE_B_1x128 = 4,    /* GEMM: B has one scale per (column, K-block)  */
   FP8Q_NO_PROMOTION = 8,     /* GEMM: accumulate all of K in the tensor core */
   FP8Q_OUT_BF16 = 16,        /* GEMM: bf16 output (default float32)          */
-  FP8Q_W_KN_LAYOUT = 32      /* quant_w: codes kept [K][N] (Dgrad operand)   */
+  FP8Q_W_KN_LAYOUT = 32,     /* quant_w: codes kept [K][N] (Dgrad operand)   */
+  FP8Q_MX_BLOCK_SCALE = 64   /* GEMM: tensor-core block scaling (UE8M0)      */
 };
 
 /*
@@ -155,6 +156,16 @@ fp8q_status fp8q_requant_1x128_to_128x1(const uint8_t* q_in, const float* s_in, 
  * FP8Q_NO_PROMOTION: the whole K is accumulated in the tensor core and the
  *      scales of K-block 0 are applied once at the end; correct only when the
  *      scales are constant along K (the accumulation study's variant).
+ * FP8Q_MX_BLOCK_SCALE: the microscaling variant [FOOLED and WHY-BE, paragraph
+ *      relating the tile/block scaling to microscaling formats on Blackwell
+ *      tensor cores]. The scales are applied inside the tensor core
+ *      (tcgen05.mma kind::mxf8f6f4, one UE8M0 scale per 32 K of each row of A
+ *      and of B, each 128-K scale repeated over its four 32-K slices) and all
+ *      of K accumulates in tensor memory: same D up to the accumulation's
+ *      rounding, no promotion. Every scale must be a positive normal power of
+ *      two (quantize with FP8Q_POW2_SCALE); any other scale is reported by
+ *      fp8q_get_status as FP8Q_ERR_INVALID_ARG and only its exponent is used.
+ *      Not combinable with FP8Q_NO_PROMOTION.
  * M >= 0 (any value), N > 0 with N % 128 == 0, K > 0 with K % 128 == 0,
  * ldd >= N. A, B, D 16-byte aligned; sa, sb 4-byte aligned.
  */
@@ -174,7 +185,7 @@ fp8q_status fp8q_gemm_blockscaled(const uint8_t* A, const float* sa, const uint8
  *             reported by fp8q_get_status as FP8Q_ERR_INVALID_ARG.
  * B         : uint8 codes [E][N][K]; sb float32 [E][K/128][N/128].
  * D         : [Mtot][N] contiguous, float32 or bf16 (FP8Q_OUT_BF16).
- * 1 <= E <= 1024. Flags: FP8Q_OUT_BF16 | FP8Q_NO_PROMOTION.
+ * 1 <= E <= 1024. Flags: FP8Q_OUT_BF16 | FP8Q_NO_PROMOTION | FP8Q_MX_BLOCK_SCALE.
  */
 fp8q_status fp8q_grouped_gemm(const uint8_t* A, const float* sa, const int32_t* m_offsets,
                               int E, const uint8_t* B, const float* sb, int64_t Mtot, int64_t N,
@@ -190,7 +201,8 @@ fp8q_status fp8q_grouped_gemm(const uint8_t* A, const float* sa, const int32_t* 
  * A         : uint8 codes [T][K] (token order), sa float32 [K/128][T].
  * row_index : DEVICE int32 [Mtot], each in [0, T); indices outside are clamped
  *             and reported by fp8q_get_status as FP8Q_ERR_INVALID_ARG.
- * m_offsets, B, sb, D, flags: as fp8q_grouped_gemm (D in expert order).
+ * m_offsets, B, sb, D, flags: as fp8q_grouped_gemm (D in expert order), except
+ * FP8Q_MX_BLOCK_SCALE, which returns FP8Q_ERR_UNSUPPORTED here.
  * T > 0 when Mtot > 0; row_index 4-byte aligned.
  */
 fp8q_status fp8q_grouped_gemm_gather(const uint8_t* A, const float* sa, int64_t T,
@@ -202,8 +214,8 @@ fp8q_status fp8q_grouped_gemm_gather(const uint8_t* A, const float* sa, int64_t 
  * Synchronizes `stream`, then reports (and clears) errors that kernels of the
  * current device recorded: FP8Q_ERR_TIMEOUT if a pipeline wait exceeded its
  * limit (the kernel stopped early: its outputs are invalid, the context stays
- * usable), FP8Q_ERR_INVALID_ARG for malformed grouped-GEMM offsets or gather
- * indices,
+ * usable), FP8Q_ERR_INVALID_ARG for malformed grouped-GEMM offsets, gather
+ * indices or (FP8Q_MX_BLOCK_SCALE) scales that are not powers of two,
  * FP8Q_ERR_CUDA if the stream reported a CUDA error. No counterpart in the
  * pages: this is the library's failure-detection hook.
  * Tuning: FP8Q_GEMM_TILE_N=128 selects 128x128 CTA tiles (four TMEM

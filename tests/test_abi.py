@@ -95,3 +95,19 @@ def test_gemm_host_validation(lib):
     assert gg(FAKE, FAKE, FAKE, 2000, FAKE, FAKE, 64, 128, 128, FAKE, 0, NULL) == lib.ERR_SHAPE
     # the 1x128 B-scale mode belongs to the dense GEMM only
     assert gg(FAKE, FAKE, FAKE, 4, FAKE, FAKE, 64, 128, 128, FAKE, 4, NULL) == lib.ERR_INVALID_ARG
+
+
+def test_mx_flag_host_validation(lib):
+    """FP8Q_MX_BLOCK_SCALE: not with FP8Q_NO_PROMOTION, not with the row
+    gather, and no other unknown flag bit is accepted."""
+    L = lib.LIB
+    g = L.fp8q_gemm_blockscaled
+    mx, nop = lib.MX_BLOCK_SCALE, lib.NO_PROMOTION
+    assert g(FAKE, FAKE, FAKE, FAKE, 16, 128, 128, FAKE, 128, mx | nop, NULL) == lib.ERR_INVALID_ARG
+    assert g(FAKE, FAKE, FAKE, FAKE, 16, 128, 128, FAKE, 128, 128, NULL) == lib.ERR_INVALID_ARG
+    assert g(NULL, NULL, NULL, NULL, 0, 128, 128, NULL, 128, mx, NULL) == lib.OK  # M == 0
+    gg = L.fp8q_grouped_gemm
+    assert gg(FAKE, FAKE, FAKE, 4, FAKE, FAKE, 64, 128, 128, FAKE, mx | nop, NULL) == lib.ERR_INVALID_ARG
+    gat = L.fp8q_grouped_gemm_gather
+    assert gat(FAKE, FAKE, 64, FAKE, FAKE, 4, FAKE, FAKE, 64, 128, 128, FAKE, mx, NULL) == \
+        lib.ERR_UNSUPPORTED
