@@ -3,7 +3,8 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload dense_fwd|square|dgrad|moe|moe_scatter|moe_gather|
-                                moe_decode|moe_act_grad|wgrad|ksweep|quant]
+                                moe_decode|moe_act_grad|wgrad|ksweep|quant|
+                                mx|mx_square|moe_mx|moe_decode_mx]
                     [--legs device,e2e,cpu]
 
 Default workload (one "step" = the whole forward hot path of an FP8 Linear):
@@ -68,7 +69,7 @@ def parse_args(argv=None):
     ap.add_argument("--workload", default="dense_fwd",
                     choices=["dense_fwd", "square", "dgrad", "moe", "moe_scatter", "moe_gather",
                              "moe_decode", "moe_act_grad", "wgrad", "ksweep", "quant", "mx",
-                             "mx_square", "moe_mx"])
+                             "mx_square", "moe_mx", "moe_decode_mx"])
     ap.add_argument("--legs", default="device,e2e,cpu",
                     help="measurement legs to run: device (always), e2e, cpu")
     a = ap.parse_args(argv)
@@ -306,10 +307,12 @@ class MoeGrouped(Workload):
         self.flops = problem.flops
         gemm = ("grouped_gemm_mx" if mx else "grouped_gemm", "tensor", problem.flops)
         if decode:  # weight-bandwidth bound: algorithmic bytes of codes, scales and D
-            gemm = ("grouped_gemm", "hbm",
+            gemm = ("grouped_gemm_mx" if mx else "grouped_gemm", "hbm",
                     E * N * K + problem.rows * K + problem.rows * N * 2
                     + E * (K // 128) * (N // 128) * 4 + (K // 128) * problem.rows * 4)
-            self.name = problem.name + " (decode: few rows per expert, weight-bandwidth bound)"
+            self.name = problem.name + " (decode: few rows per expert, weight-bandwidth bound" + (
+                "; power-of-two weight scales, UE8M0 block scaling in the tensor core)" if mx
+                else ")")
         self.kernels = [("quant_act_1x128_pow2", "hbm", problem.tokens * K * (2 + 1 + 4 / 128)),
                         gemm]
         if scatter:  # reads the tokens once, writes every routed copy
@@ -526,6 +529,8 @@ def make_workload(name, device):
         return MoeGrouped(W.MoeProblem(), device, gather=True)
     if name == "moe_decode":
         return MoeGrouped(W.MOE_DECODE, device, decode=True)
+    if name == "moe_decode_mx":
+        return MoeGrouped(W.MOE_DECODE, device, decode=True, mx=True)
     if name == "moe_act_grad":
         return MoeActGrad(W.MoeActGradProblem(), device)
     if name == "wgrad":
