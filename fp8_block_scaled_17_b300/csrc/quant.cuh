@@ -177,15 +177,19 @@ __global__ void __launch_bounds__(256) quant_rows_1x128_kernel(
   };
   const int64_t n_rb = (M + kRowUnitRows - 1) / kRowUnitRows;
 
+  // Row hw + 16 i of a unit: one 64-bit address per unit, then steps of 16 rows.
+  const int64_t ldx16 = 16 * ldx;
+  const uint32_t ring_lane = ring + (hw * 16 + l) * 16;
   auto issue = [&](const Pos& q, int stage) {
     if (q.rb < n_rb) {
+      const int64_t r0 = q.rb * kRowUnitRows + hw;
+      const __nv_bfloat16* src = x + r0 * ldx + q.kb * 128 + l * 8;
+      const uint32_t dst = ring_lane + static_cast<uint32_t>(stage) * (kRowUnitRows * 256);
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const int rr = hw + 16 * i;
-        const int64_t r = q.rb * kRowUnitRows + rr;
-        const bool ok = r < M;
-        const __nv_bfloat16* src = ok ? x + r * ldx + q.kb * 128 + l * 8 : x;
-        cp_async_16(ring + ((stage * kRowUnitRows + rr) * 16 + l) * 16, src, ok ? 16u : 0u);
+        const bool ok = r0 + 16 * i < M;
+        cp_async_16(dst + i * (16 * 256), ok ? src : x, ok ? 16u : 0u);
+        src += ldx16;
       }
     }
     cp_async_commit();
@@ -233,6 +237,9 @@ __global__ void __launch_bounds__(256) quant_rows_1x128_kernel(
     const int mine = l & 3;
     const TileScale<kPow2> ts(mine == 0 ? amax[0] : mine == 1 ? amax[1] : mine == 2 ? amax[2]
                                                                                   : amax[3]);
+    // this lane's output position in row row0 + hw; rows hw + 16 i follow in steps
+    uint8_t* qrow = q + (row0 + hw) * ldq + kb * 128 + l * 8;
+    float* sarow = sa + static_cast<int64_t>(kb) * (kScatter ? Mq : M) + row0 + hw;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int rr = hw + 16 * i;
@@ -243,8 +250,8 @@ __global__ void __launch_bounds__(256) quant_rows_1x128_kernel(
       out.y = quant4f(fi, f[i][4], f[i][5], f[i][6], f[i][7]);
       if (r < M) {
         if (!kScatter) {
-          *reinterpret_cast<uint2*>(q + r * ldq + kb * 128 + l * 8) = out;
-          if (l == i) sa[static_cast<int64_t>(kb) * M + r] = ts.s;  // lane i holds tile i's scale
+          *reinterpret_cast<uint2*>(qrow) = out;
+          if (l == i) sarow[16 * i] = ts.s;  // lane i holds tile i's scale
         } else {
           for (int j = 0; j < topk; ++j) {
             const int64_t d = __ldg(dest + r * topk + j);
@@ -255,6 +262,7 @@ __global__ void __launch_bounds__(256) quant_rows_1x128_kernel(
           }
         }
       }
+      qrow += 16 * ldq;
     }
     advance(cur);
   }
