@@ -309,34 +309,53 @@ __global__ void __launch_bounds__(256, 2) quant_cols_kernel(
   const int lane = t & 31;
   const int warp = t >> 5;
   const int64_t ncb = (Cc + 127) / 128;
-  const int64_t n_tiles = ncb * (R / 128);
   const uint32_t ring = smem_u32(smem);
   const uint32_t srow_ring = ring + kColStages * kTile;
 
-  // tile u -> column block u % ncb, row block u / ncb
-  auto issue = [&](int64_t u, int stage) {
-    if (u < n_tiles) {
-      const int64_t c0 = (u % ncb) * 128, r0 = (u / ncb) * 128;
+  // Tile u is (row block u / ncb, column block u % ncb). A CTA visits tiles
+  // u0, u0 + G, ...: the pair of its next tile is advanced by (G / ncb, G % ncb)
+  // with a carry, so no 64-bit division runs per tile.
+  struct Pos {
+    int64_t rb, cb;
+  };
+  const int64_t n_rb = R / 128;
+  const int64_t G = gridDim.x;
+  const int64_t g_rb = G / ncb, g_cb = G % ncb;
+  auto advance = [&](Pos& q) {
+    q.rb += g_rb;
+    q.cb += g_cb;
+    if (q.cb >= ncb) {
+      q.cb -= ncb;
+      ++q.rb;
+    }
+  };
+  // Rows (t >> 4) + 16 i of a tile: one 64-bit address per tile, then steps of 16 rows.
+  const int64_t ldin16 = 16 * ldin;
+  auto issue = [&](const Pos& q, int stage) {
+    if (q.rb < n_rb) {
+      const int64_t c0 = q.cb * 128, r0 = q.rb * 128;
       const uint32_t dst = ring + stage * kTile;
+      const int j = t & 15;
       if (kIn == 0) {
         const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(in);
-        const int j = t & 15;
         const int64_t cj = c0 + 8 * j;
         const int64_t valid = Cc - cj;  // bf16 elements of this chunk inside the matrix
         const uint32_t bytes = valid >= 8 ? 16u : valid > 0 ? static_cast<uint32_t>(2 * valid) : 0u;
+        const __nv_bfloat16* p = src + (r0 + (t >> 4)) * ldin + cj;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const int r = (t >> 4) + 16 * i;
-          const __nv_bfloat16* p = bytes ? src + (r0 + r) * ldin + cj : src;
-          cp_async_16(dst + (r * 16 + (j ^ ((r >> 3) & 7))) * 16, p, bytes);
+          cp_async_16(dst + (r * 16 + (j ^ ((r >> 3) & 7))) * 16, bytes ? p : src, bytes);
+          p += ldin16;
         }
       } else {
-        const uint8_t* src = static_cast<const uint8_t*>(in);
-        const int j = t & 15;  // 8-byte unit of the row
+        // 8-byte unit j of the row
+        const uint8_t* p = static_cast<const uint8_t*>(in) + (r0 + (t >> 4)) * ldin + c0 + 8 * j;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const int r = (t >> 4) + 16 * i;
-          cp_async_8(dst + (r * 16 + (j ^ ((r >> 3) & 15))) * 8, src + (r0 + r) * ldin + c0 + 8 * j);
+          cp_async_8(dst + (r * 16 + (j ^ ((r >> 3) & 15))) * 8, p);
+          p += ldin16;
         }
         if (t < 32) cp_async_16(srow_ring + stage * 512 + 16 * t, s_in + (c0 / 128) * R + r0 + 4 * t, 16u);
       }
@@ -344,19 +363,22 @@ __global__ void __launch_bounds__(256, 2) quant_cols_kernel(
     cp_async_commit();
   };
 
-  const int64_t u0 = blockIdx.x, G = gridDim.x;
+  Pos cur{static_cast<int64_t>(blockIdx.x) / ncb, static_cast<int64_t>(blockIdx.x) % ncb};
+  Pos nxt = cur;
 #pragma unroll
-  for (int s = 0; s < kColStages - 1; ++s) issue(u0 + s * G, s);
-  for (int64_t k = 0;; ++k) {
-    const int64_t u = u0 + k * G;
-    if (u >= n_tiles) break;
+  for (int s = 0; s < kColStages - 1; ++s) {
+    issue(nxt, s);
+    advance(nxt);
+  }
+  for (int64_t k = 0; cur.rb < n_rb; ++k, advance(cur)) {
     __syncthreads();  // everyone is done with the buffer the next issue overwrites
-    issue(u + (kColStages - 1) * G, static_cast<int>((k + kColStages - 1) % kColStages));
+    issue(nxt, static_cast<int>((k + kColStages - 1) % kColStages));
+    advance(nxt);
     cp_async_wait<kColStages - 1>();
     __syncthreads();  // tile u has landed, all threads' chunks
     const int stage = static_cast<int>(k % kColStages);
     const uint4* tile = reinterpret_cast<const uint4*>(smem + stage * kTile);
-    const int64_t cb = u % ncb, rb = u / ncb;
+    const int64_t cb = cur.cb, rb = cur.rb;
     const int64_t c0 = cb * 128, r0 = rb * 128;
 
     if (kIn == 0) {
@@ -407,6 +429,7 @@ __global__ void __launch_bounds__(256, 2) quant_cols_kernel(
         if ((lane & 1) == 0 && c < Cc) s_out[rb * Cc + c] = ts.s;
         fcol = ts.f;
       }
+      uint8_t* orow = out + (c0 + 8 * cg) * ldo + r0 + 8 * rg;  // output row of column e = 0
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         const float f = kBlock ? fblk : __shfl_sync(0xffffffffu, fcol, colmax_src(lane, e));
@@ -418,7 +441,8 @@ __global__ void __launch_bounds__(256, 2) quant_cols_kernel(
         uint2 o;
         o.x = quant4f(f, xv[0], xv[1], xv[2], xv[3]);
         o.y = quant4f(f, xv[4], xv[5], xv[6], xv[7]);
-        if (c < Cc) *reinterpret_cast<uint2*>(out + c * ldo + r0 + 8 * rg) = o;
+        if (c < Cc) *reinterpret_cast<uint2*>(orow) = o;
+        orow += ldo;
       }
     } else {
       const float* srow = reinterpret_cast<const float*>(smem + kColStages * kTile + stage * 512);
@@ -454,14 +478,15 @@ __global__ void __launch_bounds__(256, 2) quant_cols_kernel(
       // lane (its colmax8 column), then the factors are broadcast
       const TileScale<kPow2> ts(colmax8(a, lane));
       if ((lane & 1) == 0) s_out[rb * Cc + c0 + 8 * cg + colmax_col(lane)] = ts.s;
+      uint8_t* orow = out + (c0 + 8 * cg) * ldo + r0 + 8 * rg;  // output row of column e = 0
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         const float f = __shfl_sync(0xffffffffu, ts.f, colmax_src(lane, e));
-        const int64_t c = c0 + 8 * cg + e;
         uint2 o;
         o.x = quant4f(f, x[0][e], x[1][e], x[2][e], x[3][e]);
         o.y = quant4f(f, x[4][e], x[5][e], x[6][e], x[7][e]);
-        *reinterpret_cast<uint2*>(out + c * ldo + r0 + 8 * rg) = o;
+        *reinterpret_cast<uint2*>(orow) = o;
+        orow += ldo;
       }
     }
   }
@@ -491,36 +516,55 @@ __global__ void __launch_bounds__(256, 2) quant_blocks_kn_kernel(
   const int lane = t & 31, warp = t >> 5;
   const int hw = t >> 4, l = t & 15;
   const int64_t ncb = N / 128, nrb = K / 128;
-  const int64_t n_tiles = ncb * nrb;
   const uint32_t ring = smem_u32(smem);
 
-  // block u -> row block u / ncb, column block u % ncb (one division per 16384 values)
-  auto issue = [&](int64_t u, int stage) {
-    if (u < n_tiles) {
-      const int64_t rb = u / ncb, cb = u % ncb;
-      const __nv_bfloat16* src = in + rb * 128 * N + cb * 128 + l * 8;
+  // Block u is (row block u / ncb, column block u % ncb). A CTA visits blocks
+  // u0, u0 + G, ...: the pair of its next block is advanced by (G / ncb, G % ncb)
+  // with a carry, so no 64-bit division runs per block.
+  struct Pos {
+    int64_t rb, cb;
+  };
+  const int64_t G = gridDim.x;
+  const int64_t g_rb = G / ncb, g_cb = G % ncb;
+  auto advance = [&](Pos& q) {
+    q.rb += g_rb;
+    q.cb += g_cb;
+    if (q.cb >= ncb) {
+      q.cb -= ncb;
+      ++q.rb;
+    }
+  };
+  // rows hw + 16 i of a block: one 64-bit address per block, then steps of 16 rows
+  const int64_t n16 = 16 * N;
+  auto issue = [&](const Pos& q, int stage) {
+    if (q.rb < nrb) {
+      const __nv_bfloat16* src = in + (q.rb * 128 + hw) * N + q.cb * 128 + l * 8;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int r = hw + 16 * i;
-        cp_async_16(ring + stage * kBlkTileBytes + (r * 16 + l) * 16, src + r * N, 16u);
+        cp_async_16(ring + stage * kBlkTileBytes + (r * 16 + l) * 16, src, 16u);
+        src += n16;
       }
     }
     cp_async_commit();
   };
 
-  const int64_t u0 = blockIdx.x, G = gridDim.x;
+  Pos cur{static_cast<int64_t>(blockIdx.x) / ncb, static_cast<int64_t>(blockIdx.x) % ncb};
+  Pos nxt = cur;
 #pragma unroll
-  for (int st = 0; st < kBlkStages - 1; ++st) issue(u0 + st * G, st);
-  for (int64_t k = 0;; ++k) {
-    const int64_t u = u0 + k * G;
-    if (u >= n_tiles) break;
+  for (int st = 0; st < kBlkStages - 1; ++st) {
+    issue(nxt, st);
+    advance(nxt);
+  }
+  for (int64_t k = 0; cur.rb < nrb; ++k, advance(cur)) {
     __syncthreads();  // the buffer the next issue overwrites, and red[], are free
-    issue(u + (kBlkStages - 1) * G, static_cast<int>((k + kBlkStages - 1) % kBlkStages));
+    issue(nxt, static_cast<int>((k + kBlkStages - 1) % kBlkStages));
+    advance(nxt);
     cp_async_wait<kBlkStages - 1>();
     __syncthreads();  // block u has landed, all threads' chunks
     const int stage = static_cast<int>(k % kBlkStages);
     const uint4* tile = reinterpret_cast<const uint4*>(smem + stage * kBlkTileBytes);
-    const int64_t rb = u / ncb, cb = u % ncb;
+    const int64_t rb = cur.rb, cb = cur.cb;
 
     uint4 v[8];  // rows hw + 16 i, columns 8 l .. 8 l + 7
 #pragma unroll
@@ -541,13 +585,15 @@ __global__ void __launch_bounds__(256, 2) quant_blocks_kn_kernel(
     for (int w2 = 1; w2 < 8; ++w2) bm = fmaxf(bm, red[w2]);
     const TileScale<kPow2> ts(bm);
     if (t == 0) s_out[cb * nrb + rb] = ts.s;
+    uint8_t* orow = out + (rb * 128 + hw) * N + cb * 128 + l * 8;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
       uint2 o;
       o.x = quant4(ts, bf16_lo(w[0]), bf16_hi(w[0]), bf16_lo(w[1]), bf16_hi(w[1]));
       o.y = quant4(ts, bf16_lo(w[2]), bf16_hi(w[2]), bf16_lo(w[3]), bf16_hi(w[3]));
-      *reinterpret_cast<uint2*>(out + (rb * 128 + hw + 16 * i) * N + cb * 128 + l * 8) = o;
+      *reinterpret_cast<uint2*>(orow) = o;
+      orow += n16;
     }
   }
   cp_async_wait<0>();
