@@ -55,7 +55,9 @@ METRIC = ("FP8 block-scaled GEMM TFLOP/s (% B300 FP8 peak); "
 # an entry is removed whenever that kernel changes.
 TRAFFIC: dict = {
     # gemm_blockscaled_kernel<256>, dense forward 8192x7168x7168, bf16 out
-    ("dense_fwd", "gemm_blockscaled"): 253777664 + 95476736,
+    ("dense_fwd", "gemm_blockscaled"): 256641792 + 95580672,
+    # quant_cols_kernel<0,0,0>, dY [16384][7168] transposed 1x128, each quantizer alone
+    ("quant", "quant_act_1x128_transposed"): 234918656 + 79132928,
 }
 
 
