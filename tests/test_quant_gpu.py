@@ -196,3 +196,40 @@ def test_moe_activation_gradient_pow2_sampled(F):
     idx = torch.as_tensor(rows, device="cuda")
     rq, rs = O.quant_act_1x128(g[torch.as_tensor(rows)].float().numpy(), True)
     _assert_same(q.index_select(0, idx), s.index_select(1, idx), rq, rs)
+
+
+# ------------------------------------ more tile columns than persistent CTAs
+# The persistent quantizers advance each CTA's (row block, column block) position
+# by the grid size with a carry; with more column blocks (or K-blocks) than CTAs
+# the row step is zero and every advance carries. 512 blocks across exceeds
+# the grids these kernels launch on a 148-SM GPU (444 CTAs for rows, 296 for
+# columns and blocks).
+@pytest.mark.parametrize("pow2", [False, True])
+def test_quant_act_rows_wide(F, pow2):
+    x = W.bf16_normal((70, 512 * 128), 1.0, seed=21, outlier_frac=0.001, outlier_scale=40.0)
+    q, sa = F.quant_act_1x128(x.cuda(), pow2)
+    _assert_same(q, sa, *O.quant_act_1x128(x.float().numpy(), pow2))
+
+
+def test_quant_act_transposed_input_wide(F):
+    xt = W.bf16_normal((256, 512 * 128), 1e-3, seed=22)   # 512 column blocks of tokens
+    q, s = F.quant_act_1x128(xt.cuda(), False, transposed_input=True)
+    _assert_same(q, s, *O.quant_act_1x128_transposed_input(xt.float().numpy(), False))
+
+
+@pytest.mark.parametrize("kn_layout", [False, True])
+def test_quant_w_wide(F, kn_layout):
+    w = W.bf16_normal((256, 512 * 128), 0.02, seed=23, outlier_frac=0.001, outlier_scale=50.0)
+    q, sb = F.quant_w_128x128(w.cuda(), False, kn_layout=kn_layout)
+    rq, rs = O.quant_w_128x128(w.float().numpy(), False)
+    if kn_layout:
+        rq, rs = np.ascontiguousarray(rq.T), np.ascontiguousarray(rs.T)
+    _assert_same(q, sb, rq, rs)
+
+
+def test_requant_wide(F):
+    x = W.bf16_normal((256, 512 * 128), 1.0, seed=24, outlier_frac=0.002, outlier_scale=30.0)
+    qx, sx = F.quant_act_1x128(x.cuda(), True)
+    q2, s2 = F.requant_1x128_to_128x1(qx, sx, True)
+    rq, rs = O.quant_act_1x128(x.float().numpy(), True)
+    _assert_same(q2, s2, *O.requant_1x128_to_128x1(rq, rs, True))
