@@ -32,10 +32,11 @@
 // setmaxnreg moves them (128 x 40 + 256 x 232 = 64512). The host refuses to
 // launch unless the compiled count is exactly kLaunchRegs.
 // The promotion warps only read the scale ring (two shared loads per chunk)
-// and wait for and release a ring slot once per 8 chunks; keeping the global
-// loads off them matters, since their instruction issue is what bounds the
-// kernel. Epilogue: RN to bf16 (or FP32) from registers, 32-byte stores when
-// D and its pitch are 32-byte aligned.
+// and wait for and release a ring slot once per 8 chunks. Keeping the global
+// loads off them matters: each warp's per-chunk chain (wait for the chunk,
+// TMEM loads, FMAs, release) sets the kernel's pace, and any latency added
+// to it shows up as idle tensor time. Epilogue: RN to bf16 (or FP32) from
+// registers, 32-byte stores when D and its pitch are 32-byte aligned.
 //
 // Every wait is bounded in time. A wait that gives up raises a CTA-wide abort
 // flag and the device status word; all roles then stop, the producer waits for
