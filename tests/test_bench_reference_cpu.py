@@ -1,0 +1,48 @@
+"""bench.py's reference arm (the CPU oracle timed on a bounded sample) and its
+argument checks, run on the CPU: the JSON line carries every key of the
+benchmark contract."""
+import json
+import os
+import subprocess
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _bench(*args):
+    res = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), *args],
+                         capture_output=True, text=True, cwd=ROOT, timeout=600)
+    return res.returncode, [ln for ln in res.stdout.splitlines() if ln.startswith("{")]
+
+
+def test_reference_arm_line():
+    rc, lines = _bench("--impl", "reference", "--steps", "1", "--warmup", "3")
+    assert rc == 0 and len(lines) == 1
+    d = json.loads(lines[0])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "impl", "cpu_baseline", "e2e"):
+        assert key in d, key
+    assert d["impl"] == "reference" and d["n_gpus"] == 1
+    assert d["steps"] == 1 and d["warmup"] == 3 and d["higher_is_better"] is True
+    assert d["value"] > 0 and d["unit"] == "TFLOP/s" and d["vs_baseline"] is None
+    assert "workload" in d["config"]
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["sample"]
+    assert cb["value"] == d["value"] and cb["unit"] == d["unit"]
+    e2e = d["e2e"]
+    assert e2e["value"] == d["value"] and e2e["unit"] == d["unit"]
+    assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
+
+
+def test_reference_arm_unavailable_for_other_workloads():
+    rc, lines = _bench("--impl", "reference", "--workload", "moe", "--steps", "1",
+                       "--warmup", "3")
+    assert rc == 0 and len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["unavailable"]
+
+
+def test_fewer_than_three_warmup_steps_are_rejected():
+    rc, lines = _bench("--warmup", "2")
+    assert rc == 2 and not lines
