@@ -201,3 +201,19 @@ def test_mx_long_k_accuracy(F, K):
         print(f"K={K} {name}: max|C-R|/max|R| = {O.max_relative_error(d[rows], ref):.3e}, "
               f"max|C-R|/(|a_i||b_j|) = {(err / norm).max():.3e}")
         assert_gemm_close(d[rows], ref, na, nb, "f32")
+
+
+def test_mx_injected_timeout_is_reported_and_recoverable(F, monkeypatch):
+    """A wait that nothing satisfies (FP8Q_DEBUG_INJECT_TIMEOUT) gives up after
+    its limit; every role of the block-scaled MMA kernel stops, the call is
+    reported as FP8Q_ERR_TIMEOUT, and the next call is correct."""
+    qa, sa, qb, sb = _pow2_problem(F, 256, 512, 512, seed=40)
+    assert F.get_status() == F.OK
+    monkeypatch.setenv("FP8Q_DEBUG_INJECT_TIMEOUT", "1")
+    F.gemm_blockscaled(qa, sa, qb, sb, out_dtype=torch.float32, mx=True)
+    assert F.get_status() == F.ERR_TIMEOUT
+    assert F.get_status() == F.OK  # reading clears it
+    monkeypatch.delenv("FP8Q_DEBUG_INJECT_TIMEOUT")
+    d = F.gemm_blockscaled(qa, sa, qb, sb, out_dtype=torch.float32, mx=True)
+    assert F.get_status() == F.OK
+    _check(d, qa, sa, qb, sb, "f32")
